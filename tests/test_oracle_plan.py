@@ -1,0 +1,197 @@
+"""The oracle planner against the pages' worked example and the invariants
+the scheduling argument fixes, plus planted mistakes it must catch (CPU)."""
+import importlib.util
+import itertools
+import math
+import sys
+
+import numpy as np
+import pytest
+
+from conftest import golden
+from oracle import plan as oplan
+
+
+
+def pin_lpt_worked_example(pl):
+    """Overview ⑨: KV [1000,100,100,50], 4 CTAs, cost = KV length."""
+    g = golden("lpt_worked_example.json")
+    names = "ABCD"
+    p = pl.plan([1] * 4, g["kv_lens"], 1, 1, 1, g["num_ctas"], 1, False, alpha=g["alpha"], beta=g["beta"])
+    pr = g["printed"]
+    assert p.total_work == pr["total_work"] and p.chunk_len == pr["chunk_len"], (p.total_work, p.chunk_len)
+    got = [[[names[it.b], it.kv_end - it.kv_start] for it in q] for q in p.queues]
+    assert got == pr["cta_queues_as_request_and_length"], got
+    assert p.cta_cost[3] == pr["cta3_total"]
+    a_chunks = sorted([it for q in p.queues for it in q if it.b == 0], key=lambda it: it.kv_start)
+    assert [it.kv_end - it.kv_start for it in a_chunks] == pr["chunks_of_A"]
+    # the cost model of the source (2 qo_len + kv_len) leaves this assignment unchanged
+    p2 = pl.plan([1] * 4, g["kv_lens"], 1, 1, 1, g["num_ctas"], 1, False)
+    assert [[(it.b, it.kv_start, it.kv_end) for it in q] for q in p2.queues] == \
+           [[(it.b, it.kv_start, it.kv_end) for it in q] for q in p.queues]
+
+
+def pin_capacity_formula(pl):
+    """Technical review eq 13: 2 C T_q H_q (d + 1) = 13,209,600 for C=100, T_q=16, H_q=32, d=128."""
+    g = golden("partial_capacity.json")
+    e = pl.partial_capacity_elements(g["C"], g["T_q"], g["H_q"], g["d"])
+    assert e == g["printed"]["elements"]
+    assert round(e * 4 / 2**20, 1) == g["printed"]["mib_at_4_bytes"]
+
+
+def _cases():
+    rng = np.random.default_rng(7)
+    cases = []
+    for i in range(40):
+        B = int(rng.integers(1, 9))
+        causal = bool(i % 2)
+        decode = i % 3 == 0
+        g = int(rng.choice([1, 2, 4]))
+        kv = rng.integers(0, 300, size=B)
+        qo = np.ones(B, int) if decode else np.minimum(kv, rng.integers(1, 60, size=B)) if causal else rng.integers(1, 60, size=B)
+        qo = np.maximum(qo, 1)
+        tile = g if decode else int(rng.choice([16, 32])) * g
+        cases.append(dict(qo=qo.tolist(), kv=kv.tolist(), hk=int(rng.integers(1, 4)), g=g, tile=tile,
+                          C=int(rng.integers(1, 20)), ps=int(rng.choice([1, 4, 16])), causal=causal))
+    return cases
+
+
+def pin_coverage(pl):
+    """Every (request, kv head, query position, visible KV position) is covered
+    exactly once, and each multi-chunk output's slots are consecutive and in
+    ascending chunk order (walkthrough §VIII.5 reduction map)."""
+    for c in _cases():
+        p = pl.plan(c["qo"], c["kv"], c["hk"], c["g"], c["tile"], c["C"], c["ps"], c["causal"])
+        items = [it for q in p.queues for it in q]
+        by_out = {}
+        for it in items:
+            by_out.setdefault((it.b, it.tile, it.kv_head), []).append(it)
+        for b in range(len(c["qo"])):
+            ntile = -(-c["qo"][b] * c["g"] // c["tile"])
+            for t in range(ntile):
+                per = c["tile"] // c["g"]
+                last_pos = min(c["qo"][b], (t + 1) * per) - 1
+                vis = c["kv"][b] if not c["causal"] else max(0, min(c["kv"][b], last_pos + c["kv"][b] - c["qo"][b] + 1))
+                for h in range(c["hk"]):
+                    chunks = sorted(by_out.pop((b, t, h)), key=lambda it: it.kv_start)
+                    covered = [x for it in chunks for x in range(it.kv_start, it.kv_end)]
+                    assert covered == list(range(vis)), (c, b, t, h)
+                    assert all(it.kv_end - it.kv_start <= p.chunk_len for it in chunks)
+                    assert all(it.kv_start % c["ps"] == 0 for it in chunks)
+                    if len(chunks) == 1:
+                        assert chunks[0].slot == -1
+                    else:
+                        slots = [it.slot for it in chunks]
+                        assert slots == list(range(slots[0], slots[0] + len(chunks)))
+        assert not by_out
+        # reduction map: outputs in (b, tile, kv_head) order with consecutive slot ranges
+        nxt = 0
+        for o in p.outputs:
+            assert o.slot_begin == nxt and o.n_slots >= 2
+            nxt += o.n_slots
+        assert nxt == p.num_partials
+
+
+def pin_chunk_len_and_bounds(pl):
+    """L = max(1, ceil(W / C)) rounded up to a page (technical review Algorithm 2
+    step 4); partial slots stay within 2 C (eq 13's factor of two, per tile and
+    kv head); the makespan is at least eq 12's bound."""
+    for c in _cases():
+        p = pl.plan(c["qo"], c["kv"], c["hk"], c["g"], c["tile"], c["C"], c["ps"], c["causal"])
+        W = sum(-(-q * c["g"] // c["tile"]) * k * c["hk"] for q, k in zip(c["qo"], c["kv"]))
+        assert p.total_work == W
+        L = max(1, math.ceil(W / c["C"]))
+        assert p.chunk_len == math.ceil(L / c["ps"]) * c["ps"]
+        assert p.num_partials <= 2 * c["C"]
+        costs = []
+        for q in p.queues:
+            for it in q:
+                lq = min(c["qo"][it.b], (it.tile + 1) * (c["tile"] // c["g"])) - it.tile * (c["tile"] // c["g"])
+                costs.append(2 * lq + (it.kv_end - it.kv_start))
+        assert max(p.cta_cost) >= pl.makespan_lower_bound(costs, c["C"]) - 1e-9
+        assert sum(p.cta_cost) == sum(costs)
+
+
+def pin_lpt_quality(pl):
+    """Longest-first greedy: each queue is in non-increasing chunk length order,
+    and the makespan is within Graham's (4/3 - 1/(3C)) of the optimum, checked
+    by brute force over every assignment of up to 8 chunks to up to 3 CTAs."""
+    rng = np.random.default_rng(8)
+    for _ in range(60):
+        B = int(rng.integers(1, 9))
+        C = int(rng.integers(1, 4))
+        kv = rng.integers(1, 50, size=B).tolist()
+        p = pl.plan([1] * B, kv, 1, 1, 1, C, 1, False, alpha=0, beta=1)
+        for q in p.queues:
+            lens = [it.kv_end - it.kv_start for it in q]
+            assert lens == sorted(lens, reverse=True)
+        sizes = [it.kv_end - it.kv_start for q in p.queues for it in q]
+        if len(sizes) > 8:
+            continue
+        best = min(max(sum(s for s, a in zip(sizes, asg) if a == c) for c in range(C))
+                   for asg in itertools.product(range(C), repeat=len(sizes)))
+        assert max(p.cta_cost) <= (4 / 3 - 1 / (3 * C)) * best + 1e-9, (sizes, C, p.cta_cost, best)
+
+
+def pin_determinism(pl):
+    c = _cases()[5]
+    a = pl.plan(c["qo"], c["kv"], c["hk"], c["g"], c["tile"], c["C"], c["ps"], c["causal"])
+    b = pl.plan(c["qo"], c["kv"], c["hk"], c["g"], c["tile"], c["C"], c["ps"], c["causal"])
+    assert a.queues == b.queues and a.outputs == b.outputs
+
+
+def pin_empty_tiles(pl):
+    """A request with no KV still gets one empty chunk per (tile, kv head)."""
+    p = pl.plan([1, 1], [0, 5], 2, 1, 1, 3, 4, False)
+    items = [it for q in p.queues for it in q]
+    assert sorted((it.b, it.kv_head, it.kv_start, it.kv_end) for it in items if it.b == 0) == [(0, 0, 0, 0), (0, 1, 0, 0)]
+
+
+def pin_traffic_ratio(pl):
+    """Technical review eq 15 limits: n = 1 gives 1; no suffix gives n."""
+    assert pl.prefix_traffic_ratio(1, 8192, 300) == pytest.approx(1.0)
+    assert pl.prefix_traffic_ratio(64, 8192, 0) == pytest.approx(64.0)
+
+
+ALL_PLAN_PINS = [pin_lpt_worked_example, pin_capacity_formula, pin_coverage, pin_chunk_len_and_bounds,
+                 pin_lpt_quality, pin_determinism, pin_empty_tiles, pin_traffic_ratio]
+
+
+@pytest.mark.parametrize("pin", ALL_PLAN_PINS, ids=lambda f: f.__name__)
+def test_plan_pin(pin):
+    pin(oplan)
+
+
+PLAN_MUTATIONS = [
+    ("floor_chunk", "L = max(1, -(-W // num_ctas))", "L = max(1, W // num_ctas)"),
+    ("no_page_rounding", "L = -(-L // page_size) * page_size", "L = L"),
+    ("shortest_first", "chunks.sort(key=lambda c: (-(c[4] - c[3]), c[0], c[1], c[2], c[3]))",
+     "chunks.sort(key=lambda c: ((c[4] - c[3]), c[0], c[1], c[2], c[3]))"),
+    ("heap_sign_flipped", "heapq.heappush(heap, (cost + alpha * lq + beta * (e - s), cta))",
+     "heapq.heappush(heap, (cost - alpha * lq - beta * (e - s), cta))"),
+    ("causal_top_left", "return max(0, min(kv_len, last_pos + kv_len - qo_len + 1))",
+     "return max(0, min(kv_len, last_pos + 1))"),
+    ("no_head_factor", "W += kv_lens[b]", "W += kv_lens[b] if h == 0 else 0"),
+    ("no_empty_chunk", "or [(0, 0)]", "or []"),
+    ("slots_not_consecutive", "chunks.append((b, t, h, s, e, lq, next_slot + i))",
+     "chunks.append((b, t, h, s, e, lq, next_slot + 2 * i))"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", PLAN_MUTATIONS, ids=[m[0] for m in PLAN_MUTATIONS])
+def test_plan_pins_catch_planted_mistake(name, old, new, tmp_path):
+    src = open(oplan.__file__).read()
+    assert src.count(old) == 1, name
+    path = tmp_path / f"plan_{name}.py"
+    path.write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location(f"plan_mutant_{name}", path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[spec.name] = mod
+    spec.loader.exec_module(mod)
+    caught = []
+    for pin in ALL_PLAN_PINS:
+        try:
+            pin(mod)
+        except Exception:
+            caught.append(pin.__name__)
+    assert caught, name
