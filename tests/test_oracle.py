@@ -1,7 +1,8 @@
 """The oracle against its pins, and planted mistakes in copies of the oracle
 that the pins must catch (all on the CPU)."""
 import os
-import re
+import subprocess
+import sys
 
 import pytest
 
@@ -37,18 +38,33 @@ MUTATIONS = [
 ]
 
 
+_RUN_PINS = """
+import sys
+sys.path[:0] = [{tests!r}, {root!r}]
+import oracle, oracle_pins
+mutant = oracle.COracle({lib!r})
+caught = []
+for pin in oracle_pins.ALL_PINS:
+    try:
+        pin(mutant)
+    except (AssertionError, ValueError):
+        caught.append(pin.__name__)
+print(",".join(caught))
+sys.exit(0 if caught else 3)
+"""
+
+
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_pins_catch_planted_mistake(name, old, new, tmp_path):
+    """The pins run in a child process: a mutant may also read out of bounds and
+    crash, which counts as caught."""
     src = open(oracle.SOURCE).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not unique"
     mutant_src = tmp_path / "attention_mutant.c"
     mutant_src.write_text(src.replace(old, new))
     lib = oracle.compile_source(str(mutant_src), str(tmp_path / "libmutant.so"))
-    mutant = oracle.COracle(lib)
-    caught = []
-    for pin in oracle_pins.ALL_PINS:
-        try:
-            pin(mutant)
-        except (AssertionError, ValueError):
-            caught.append(pin.__name__)
-    assert caught, f"no pin caught the planted mistake {name}"
+    tests_dir = os.path.dirname(os.path.abspath(__file__))
+    code = _RUN_PINS.format(tests=tests_dir, root=os.path.dirname(tests_dir), lib=lib)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode != 3, f"no pin caught the planted mistake {name}"
+    assert r.returncode == 0 or r.returncode < 0, r.stderr[-2000:]
