@@ -1,0 +1,514 @@
+// Split-KV paged decode with the g query heads of a kv head fused into one tile,
+// and the plan-driven merge of split outputs.
+//
+// Decode is HBM-bound (FlashInfer: Making Attention Fit the Serving Workload,
+// §2.2 eq 2; Engineering a Customizable, Block-Sparse Attention Engine, §II.3-4):
+// every byte of K and V is read once, and the g heads that share a kv head reuse
+// each loaded KV tile (head-group fusion, technical review eq 3; overview ⑦).
+//
+// bf16 kernel (one persistent CTA of 4 warps per plan queue):
+//   - loader: page-indexed 16-byte cp.async of K and V rows into a 3-stage
+//     shared-memory ring (sparse gather, dense compute: overview ⑥,
+//     walkthrough §IV.2 and §V.4). Stage = 64 tokens; the ring runs across the
+//     CTA's work items, so the next item's first tiles load while the current
+//     one finishes. Each thread loads one token per stage and prefetches the
+//     page index of its next token one stage early.
+//   - compute: each warp takes 16 of the 64 tokens; S = Q K^T and O += P V on
+//     the warp-level tensor-core MMA (m16n8k16, rows = the g fused heads), fp32
+//     online softmax in base 2 with the scale folded into log2(e)
+//     (walkthrough §II.2), then the four warps' states are merged in shared
+//     memory at the end of each item.
+//   - output: the final (O, LSE) when the item is its output's only chunk,
+//     else an fp32 partial state in the workspace slot the plan assigned
+//     (overview ⑨, write-through of unsplit requests).
+// Reduction kernel: the reduction map's slots of each split output, merged in
+// ascending order with a common maximum (technical review eq 6), no atomics.
+#include <cfloat>
+
+#include "bsp_internal.h"
+#include "device_common.cuh"
+
+namespace bsp {
+namespace {
+
+using namespace dev;
+
+constexpr int kDecThreads = 128;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kTileK = 64;      // KV tokens per ring stage
+constexpr int kStages = 3;
+constexpr int kMmaRows = 16;    // fused heads per tile (M of the MMA)
+
+template <int D>
+struct DecodeLayout {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kChunks = D / 8;                 // 16-byte chunks per row
+    static constexpr int kTileBytes = kTileK * kRowBytes; // K (or V) part of a stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStatBytes = kDecWarps * kMmaRows * 2 * sizeof(float);
+    static constexpr int kSmemBytes = kStages * kStageBytes + kStatBytes;
+    // The merge scratch of one item reuses a free stage: 4 warps x 16 rows x D floats.
+    static_assert(kDecWarps * kMmaRows * D * 4 <= kStageBytes, "merge scratch must fit in one stage");
+};
+
+struct DecodeParams {
+    const uint8_t *ws;
+    uint64_t off_queue, off_items, off_plse, off_po;
+    const void *q, *k, *v;
+    const int32_t *kv_indices;
+    void *o;
+    float *lse;
+    float scale_log2;
+    int H_qo, H_kv, g, page_size, tile_rows;
+};
+
+// Swizzled byte offset of 16-byte chunk c of row r inside a K or V tile:
+// chunks are XOR-permuted by the row's low 3 bits, so the 8 rows an ldmatrix
+// phase reads fall in 8 different bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (uint32_t)(r * DecodeLayout<D>::kRowBytes + ((c ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const DecodeParams p) {
+    using LY = DecodeLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
+    const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
+    const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
+    if (it0 >= it1) return;  // uniform across the CTA, before any barrier
+
+    const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
+    const uint32_t sbase = smem_u32(smem);
+
+    // ---------------- producer: walks (item, tile) in queue order ----------
+    const int ptok = tid >> 1, phalf = tid & 1;
+    int pi = it0 - 1, pt = 0, pn = 0;             // item, tile within item, tiles of item
+    int p_head = 0, p_start = 0, p_end = 0, p_base = 0;
+    bool p_has = false, p_valid = false;
+    int p_page = 0, p_off = 0;                      // prefetched address of this thread's token
+
+    auto p_advance = [&]() {
+        ++pt;
+        while (pt >= pn) {
+            ++pi;
+            if (pi >= it1) { p_has = false; return; }
+            const bsp_work_item &w = items[pi];
+            p_head = w.kv_head; p_start = w.kv_start; p_end = w.kv_end; p_base = w.page_base;
+            pn = (p_end - p_start + kTileK - 1) / kTileK;
+            pt = 0;
+        }
+        p_has = true;
+        const int t = p_start + pt * kTileK + ptok;
+        p_valid = t < p_end;
+        if (p_valid) {
+            p_page = __ldg(p.kv_indices + p_base + t / p.page_size);
+            p_off = t % p.page_size;
+        }
+    };
+    auto p_issue = [&](int buf) {
+        if (p_has) {
+            const uint32_t dk = sbase + buf * LY::kStageBytes;
+            const uint32_t dv = dk + LY::kTileBytes;
+            const size_t row = p_valid ? ((size_t)p_page * p.page_size + p_off) * p.H_kv + p_head : 0;
+            const __nv_bfloat16 *sk = kg + row * D;
+            const __nv_bfloat16 *sv = vg + row * D;
+            const int nb = p_valid ? 16 : 0;
+#pragma unroll
+            for (int i = 0; i < LY::kChunks / 2; ++i) {
+                const int c = phalf * (LY::kChunks / 2) + i;
+                cp_async_16(dk + swz<D>(ptok, c), sk + c * 8, nb);
+                cp_async_16(dv + swz<D>(ptok, c), sv + c * 8, nb);
+            }
+        }
+        cp_async_commit();
+        p_advance();
+    };
+
+    p_advance();
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) p_issue(s);
+
+    // ---------------- consumer ---------------------------------------------
+    const int g = p.g;
+    const int r0 = lane >> 2, r1 = r0 + 8;
+    float *stats = reinterpret_cast<float *>(smem + kStages * LY::kStageBytes);  // [warp][16][m, l]
+    int j = 0;  // tiles consumed so far (ring position)
+    for (int it = it0; it < it1; ++it) {
+        const bsp_work_item w = items[it];
+        const int len = w.kv_end - w.kv_start;
+        const int ntiles = (len + kTileK - 1) / kTileK;
+
+        // Q fragments of the g fused rows (rows >= g are zero)
+        uint32_t qa[D / 16][4];
+        {
+            const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q) +
+                                      ((size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g) * D;
+            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(qb + (size_t)r0 * D);
+            const uint32_t *q1 = reinterpret_cast<const uint32_t *>(qb + (size_t)r1 * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c2 = (kk * 16 + 2 * (lane & 3)) >> 1;  // index in bf16 pairs
+                qa[kk][0] = r0 < g ? __ldg(q0 + c2) : 0u;
+                qa[kk][1] = r1 < g ? __ldg(q1 + c2) : 0u;
+                qa[kk][2] = r0 < g ? __ldg(q0 + c2 + 4) : 0u;
+                qa[kk][3] = r1 < g ? __ldg(q1 + c2 + 4) : 0u;
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float acc[D / 8][4];
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+        for (int t = 0; t < ntiles; ++t, ++j) {
+            p_issue((j + kStages - 1) % kStages);
+            cp_async_wait<kStages - 1>();
+            __syncthreads();
+            const int valid = min(kTileK, len - t * kTileK) - warp * 16;  // this warp's tokens
+            if (valid > 0) {
+                const uint32_t kb = sbase + (j % kStages) * LY::kStageBytes;
+                const uint32_t vb = kb + LY::kTileBytes;
+                float s[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+                {
+                    const int mi = lane >> 3;
+                    const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(kb + swz<D>(row, kk * 2 + (mi & 1)), b0, b1, b2, b3);
+                        mma_bf16_16816(s[0], qa[kk], b0, b1);
+                        mma_bf16_16816(s[1], qa[kk], b2, b3);
+                    }
+                }
+                // scale into base 2, mask tokens past the chunk end
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int tk = n * 8 + 2 * (lane & 3) + (c & 1);
+                        s[n][c] = tk < valid ? s[n][c] * p.scale_log2 : -INFINITY;
+                    }
+                    mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+                    mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+                const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+                m0 = n0;
+                m1 = n1;
+                float ps[2][4];
+                float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    ps[n][0] = exp2f(s[n][0] - ref0);
+                    ps[n][1] = exp2f(s[n][1] - ref0);
+                    ps[n][2] = exp2f(s[n][2] - ref1);
+                    ps[n][3] = exp2f(s[n][3] - ref1);
+                    sum0 += ps[n][0] + ps[n][1];
+                    sum1 += ps[n][2] + ps[n][3];
+                }
+                l0 = l0 * a0 + sum0;
+                l1 = l1 * a1 + sum1;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    acc[n][0] *= a0; acc[n][1] *= a0;
+                    acc[n][2] *= a1; acc[n][3] *= a1;
+                }
+                uint32_t pa[4];
+                pa[0] = pack_bf16(ps[0][0], ps[0][1]);
+                pa[1] = pack_bf16(ps[0][2], ps[0][3]);
+                pa[2] = pack_bf16(ps[1][0], ps[1][1]);
+                pa[3] = pack_bf16(ps[1][2], ps[1][3]);
+                {
+                    const int mi = lane >> 3;
+                    const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                    for (int nd = 0; nd < D / 16; ++nd) {
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(vb + swz<D>(row, nd * 2 + (mi >> 1)), b0, b1, b2, b3);
+                        mma_bf16_16816(acc[2 * nd], pa, b0, b1);
+                        mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+
+        // ---- merge the four warps' states; write the output or a partial ----
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        float *scratch = reinterpret_cast<float *>(smem + ((j + kStages - 1) % kStages) * LY::kStageBytes);
+        if ((lane & 3) == 0) {
+            stats[(warp * 16 + r0) * 2 + 0] = m0;
+            stats[(warp * 16 + r0) * 2 + 1] = l0;
+            stats[(warp * 16 + r1) * 2 + 0] = m1;
+            stats[(warp * 16 + r1) * 2 + 1] = l1;
+        }
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2 *>(scratch + (warp * 16 + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(scratch + (warp * 16 + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
+        }
+        __syncthreads();
+        for (int e = tid; e < g * D; e += kDecThreads) {
+            const int row = e / D, d = e - row * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int ww = 0; ww < kDecWarps; ++ww) M = fmaxf(M, stats[(ww * 16 + row) * 2]);
+            float val = 0.f, lse_v = -INFINITY;
+            if (M != -INFINITY) {
+                float L = 0.f, num = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kDecWarps; ++ww) {
+                    const float f = exp2f(stats[(ww * 16 + row) * 2] - M);
+                    L += stats[(ww * 16 + row) * 2 + 1] * f;
+                    num += scratch[(ww * 16 + row) * D + d] * f;
+                }
+                val = num / L;
+                lse_v = (M + log2f(L)) * kLn2;
+            }
+            if (w.slot < 0) {
+                const size_t orow = (size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g + row;
+                static_cast<__nv_bfloat16 *>(p.o)[orow * D + d] = __float2bfloat16_rn(val);
+                if (d == 0 && p.lse) p.lse[orow] = lse_v;
+            } else {
+                const size_t prow = (size_t)w.slot * p.tile_rows + row;
+                reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_po)[prow * D + d] = val;
+                if (d == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
+// fp32 decode: CUDA-core fp32 arithmetic, one warp per fused row, lanes over
+// head_dim (D / 32 elements each), keys streamed from global memory.
+template <int D>
+__global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodeParams p) {
+    constexpr int E = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
+    const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
+    const float *qg = static_cast<const float *>(p.q);
+    const float *kg = static_cast<const float *>(p.k);
+    const float *vg = static_cast<const float *>(p.v);
+    for (int it = queue[blockIdx.x]; it < queue[blockIdx.x + 1]; ++it) {
+        const bsp_work_item w = items[it];
+        for (int row = warp; row < p.g; row += kDecWarps) {
+            const size_t qrow = (size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * p.g + row;
+            float qr[E], acc[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) { qr[i] = qg[qrow * D + lane + 32 * i]; acc[i] = 0.f; }
+            float m = -INFINITY, l = 0.f;
+            for (int t = w.kv_start; t < w.kv_end; ++t) {
+                const int page = __ldg(p.kv_indices + w.page_base + t / p.page_size);
+                const size_t kr = ((size_t)page * p.page_size + t % p.page_size) * p.H_kv + w.kv_head;
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < E; ++i) dot = fmaf(qr[i], kg[kr * D + lane + 32 * i], dot);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                const float x = dot * p.scale_log2;
+                const float mn = fmaxf(m, x);
+                const float a = exp2f(m - mn), pe = exp2f(x - mn);
+                l = l * a + pe;
+#pragma unroll
+                for (int i = 0; i < E; ++i) acc[i] = fmaf(pe, vg[kr * D + lane + 32 * i], acc[i] * a);
+                m = mn;
+            }
+            const bool empty = w.kv_end <= w.kv_start;
+            const float inv = empty ? 0.f : 1.f / l;
+            const float lse_v = empty ? -INFINITY : (m + log2f(l)) * kLn2;
+            if (w.slot < 0) {
+                float *o = static_cast<float *>(p.o) + qrow * D;
+#pragma unroll
+                for (int i = 0; i < E; ++i) o[lane + 32 * i] = acc[i] * inv;
+                if (lane == 0 && p.lse) p.lse[qrow] = lse_v;
+            } else {
+                const size_t prow = (size_t)w.slot * p.tile_rows + row;
+                float *po = reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_po) + prow * D;
+#pragma unroll
+                for (int i = 0; i < E; ++i) po[lane + 32 * i] = acc[i] * inv;
+                if (lane == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
+            }
+        }
+    }
+}
+
+// Merge of split outputs: one warp per (reduction-map entry, fused row).
+struct ReduceParams {
+    const uint8_t *ws;
+    uint64_t off_header, off_merges, off_plse, off_po;
+    void *o;
+    float *lse;
+    int H_qo, g, tile_rows;
+};
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
+    constexpr int E = D / 32;
+    const DevHeader *hdr = reinterpret_cast<const DevHeader *>(p.ws + p.off_header);
+    const bsp_merge_entry *merges = reinterpret_cast<const bsp_merge_entry *>(p.ws + p.off_merges);
+    const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
+    const float *po = reinterpret_cast<const float *>(p.ws + p.off_po);
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int total = hdr->num_merges * p.tile_rows;
+    for (int task = gw; task < total; task += nw) {
+        const bsp_merge_entry e = merges[task / p.tile_rows];
+        const int r = task % p.tile_rows;
+        if (r >= e.n_pos * p.g) continue;
+        float M = -INFINITY;
+        for (int s = 0; s < e.n_slots; ++s) M = fmaxf(M, plse[(size_t)(e.slot_begin + s) * p.tile_rows + r]);
+        float acc[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[i] = 0.f;
+        float L = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < e.n_slots; ++s) {
+                const size_t prow = (size_t)(e.slot_begin + s) * p.tile_rows + r;
+                const float wgt = exp2f((plse[prow] - M) * kLog2e);
+                L += wgt;
+#pragma unroll
+                for (int i = 0; i < E; ++i) acc[i] = fmaf(wgt, po[prow * D + lane * E + i], acc[i]);
+            }
+        }
+        const float inv = M != -INFINITY ? 1.f / L : 0.f;
+        const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
+        OutT *o = static_cast<OutT *>(p.o) + orow * D + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) o[i] = from_float<OutT>(acc[i] * inv);
+        if (lane == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
+    }
+}
+
+int num_sms_of_current_device(int *dev_out) {
+    static int sms[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    if (!sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        sms[dev] = n;
+    }
+    if (dev_out) *dev_out = dev;
+    return sms[dev];
+}
+
+template <int D>
+int launch_decode_bf16(const DecodeParams &p, int grid, cudaStream_t stream) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    if (num_sms_of_current_device(&dev) < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecodeLayout<D>::kSmemBytes);
+        if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
+        configured[dev] = true;
+    }
+    decode_bf16_kernel<D><<<grid, kDecThreads, DecodeLayout<D>::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
+}
+
+template <int D>
+int launch_decode_f32(const DecodeParams &p, int grid, cudaStream_t stream) {
+    decode_f32_kernel<D><<<grid, kDecThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
+}
+
+template <int D, typename OutT>
+int launch_reduce_t(const ReduceParams &p, cudaStream_t stream) {
+    const int sms = num_sms_of_current_device(nullptr);
+    if (sms < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    reduce_kernel<D, OutT><<<2 * sms, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("reduce launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
+}
+
+}  // namespace
+
+int decode_ctas_per_sm(int head_dim, int dtype) {
+    if (dtype != BSP_DTYPE_BF16) return 4;
+    return 2;  // 3 x 32 KB (D = 128) or 3 x 16 KB ring per CTA; 2 CTAs keep ~190 KB of copies in flight per SM
+}
+
+int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                  const int32_t *kv_indices, float sm_scale, void *o, float *lse, void *workspace,
+                  cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    DecodeParams p;
+    p.ws = static_cast<const uint8_t *>(workspace);
+    p.off_queue = plan->off_queue_indptr;
+    p.off_items = plan->off_items;
+    p.off_plse = plan->off_partial_lse;
+    p.off_po = plan->off_partial_o;
+    p.q = q; p.k = k_pages; p.v = v_pages;
+    p.kv_indices = kv_indices;
+    p.o = o;
+    p.lse = lse;
+    p.scale_log2 = sm_scale * kLog2e;
+    p.H_qo = P.num_qo_heads;
+    p.H_kv = P.num_kv_heads;
+    p.g = plan->group;
+    p.page_size = P.page_size;
+    p.tile_rows = plan->tile_rows;
+    const int grid = plan->capacity.num_ctas;
+    if (P.dtype == BSP_DTYPE_BF16) {
+        if (p.g > kMmaRows) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode needs num_qo_heads / num_kv_heads <= 16");
+        if (P.head_dim == 128) return launch_decode_bf16<128>(p, grid, stream);
+        if (P.head_dim == 64) return launch_decode_bf16<64>(p, grid, stream);
+        return fail(BSP_ERR_UNSUPPORTED, "bf16 decode supports head_dim 64 and 128");
+    }
+    switch (P.head_dim) {
+        case 32: return launch_decode_f32<32>(p, grid, stream);
+        case 64: return launch_decode_f32<64>(p, grid, stream);
+        case 128: return launch_decode_f32<128>(p, grid, stream);
+        case 256: return launch_decode_f32<256>(p, grid, stream);
+        default: return fail(BSP_ERR_UNSUPPORTED, "fp32 decode supports head_dim 32, 64, 128, 256");
+    }
+}
+
+int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace, cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    ReduceParams p;
+    p.ws = static_cast<const uint8_t *>(workspace);
+    p.off_header = plan->off_header;
+    p.off_merges = plan->off_merges;
+    p.off_plse = plan->off_partial_lse;
+    p.off_po = plan->off_partial_o;
+    p.o = o;
+    p.lse = lse;
+    p.H_qo = P.num_qo_heads;
+    p.g = plan->group;
+    p.tile_rows = plan->tile_rows;
+    const bool bf = P.dtype == BSP_DTYPE_BF16;
+    switch (P.head_dim) {
+        case 32: return bf ? launch_reduce_t<32, __nv_bfloat16>(p, stream) : launch_reduce_t<32, float>(p, stream);
+        case 64: return bf ? launch_reduce_t<64, __nv_bfloat16>(p, stream) : launch_reduce_t<64, float>(p, stream);
+        case 128: return bf ? launch_reduce_t<128, __nv_bfloat16>(p, stream) : launch_reduce_t<128, float>(p, stream);
+        case 256: return bf ? launch_reduce_t<256, __nv_bfloat16>(p, stream) : launch_reduce_t<256, float>(p, stream);
+        default: return fail(BSP_ERR_UNSUPPORTED, "head_dim must be 32, 64, 128 or 256");
+    }
+}
+
+}  // namespace bsp

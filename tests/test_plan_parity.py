@@ -1,0 +1,123 @@
+"""The library's C++ planner against the oracle planner: bit-exact queues,
+items and reduction map on the same lengths (host only, no device)."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import plan as oplan
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    from block_sparse_paged_gb300 import build
+    build.build()
+    import block_sparse_paged_gb300 as bsp
+    return bsp
+
+
+def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alpha=2, beta=1, D=128,
+             max_batch=None, max_qo=None):
+    qo_lens = np.asarray(qo_lens, np.int64)
+    kv_lens = np.asarray(kv_lens, np.int64)
+    B = len(kv_lens)
+    npages = np.array([-(-int(k) // page_size) for k in kv_lens], np.int64)
+    last = np.array([int(k) - (n - 1) * page_size if n > 0 else 0 for k, n in zip(kv_lens, npages)], np.int32)
+    kv_indptr = np.zeros(B + 1, np.int32)
+    kv_indptr[1:] = np.cumsum(npages)
+    qo_indptr = np.zeros(B + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(qo_lens)
+    g = H_qo // H_kv
+    prob = bsp.make_problem(mode, H_qo, H_kv, D, page_size, causal, __import__("torch").bfloat16)
+    cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]))
+    info, queue, items, merges = bsp.plan_host(prob, cap, kv_indptr, last,
+                                               None if mode == bsp.BSP_MODE_DECODE and np.all(qo_lens == 1) else qo_indptr,
+                                               alpha, beta)
+    tile = g if mode == bsp.BSP_MODE_DECODE else 128
+    ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta)
+    return info, queue, items, merges, ref, qo_indptr, kv_indptr
+
+
+def assert_same(info, queue, items, merges, ref, qo_indptr, kv_indptr):
+    assert info.chunk_len == ref.chunk_len and info.total_work == ref.total_work
+    assert info.num_partials == ref.num_partials
+    got = [[(int(it["b"]), int(it["tile"]), int(it["kv_head"]), int(it["kv_start"]), int(it["kv_end"]), int(it["slot"]))
+            for it in items[queue[c]:queue[c + 1]]] for c in range(len(queue) - 1)]
+    want = [[(it.b, it.tile, it.kv_head, it.kv_start, it.kv_end, it.slot) for it in q] for q in ref.queues]
+    assert got == want
+    got_m = [(int(m["b"]), int(m["tile"]), int(m["kv_head"]), int(m["slot_begin"]), int(m["n_slots"])) for m in merges]
+    want_m = [(o.b, o.tile, o.kv_head, o.slot_begin, o.n_slots) for o in ref.outputs]
+    assert got_m == want_m
+    # derived fields the kernels read
+    per = info.tile_rows // info.group
+    for it in items:
+        b = int(it["b"])
+        assert it["pos0"] == it["tile"] * per
+        assert it["q_tok0"] == qo_indptr[b] + it["pos0"]
+        assert it["qo_len"] == qo_indptr[b + 1] - qo_indptr[b]
+        assert it["page_base"] == kv_indptr[b]
+        assert it["n_pos"] == min(int(it["qo_len"]), int(it["pos0"]) + per) - it["pos0"]
+
+
+def test_lpt_worked_example(bsp):
+    out = run_both(bsp, bsp.BSP_MODE_DECODE, [1] * 4, [1000, 100, 100, 50], 1, 1, 1, False, 4, alpha=0, beta=1)
+    assert_same(*out)
+    q, items = out[1], out[2]
+    assert [int(items[i]["kv_end"] - items[i]["kv_start"]) for i in range(q[3], q[4])] == [100, 100, 61, 50]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_decode_and_prefill(bsp, seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 40))
+    H_kv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    ps = int(rng.choice([1, 3, 16, 64]))
+    C = int(rng.integers(1, 400))
+    kv = rng.integers(0, 5000, size=B)
+    if seed % 2 == 0:
+        out = run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(B, int), kv, ps, H_kv * g, H_kv, bool(seed % 4 == 0), C)
+    else:
+        causal = bool(seed % 3)
+        qo = np.maximum(1, np.minimum(kv, rng.integers(1, 700, size=B))) if causal else rng.integers(1, 700, size=B)
+        out = run_both(bsp, bsp.BSP_MODE_PREFILL, qo, kv, ps, H_kv * g, H_kv, causal, C)
+    assert_same(*out)
+
+
+def test_benchmark_workload_lengths(bsp):
+    b2 = workloads.batched_decode_bf16()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, b2.qo_lens, b2.kv_lens, 16, 32, 8, False, 304))
+    b4 = workloads.ragged_causal_prefill_bf16()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, b4.qo_lens, b4.kv_lens, 16, 32, 8, True, 152))
+    sp = workloads.shared_prefix_decode_bf16()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, sp.prefix.qo_lens, sp.prefix.kv_lens, 16, 32, 8, False, 152))
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, sp.suffix.qo_lens, sp.suffix.kv_lens, 16, 32, 8, False, 304))
+
+
+def test_capacity_and_metadata_errors(bsp):
+    import torch
+    prob = bsp.make_problem(bsp.BSP_MODE_DECODE, 8, 2, 128, 4, False, torch.bfloat16)
+    with pytest.raises(bsp.BspError, match="CAPACITY"):
+        bsp.plan_host(prob, bsp.Capacity(2, 8, 2), [0, 1, 2, 3], [1, 1, 1])          # batch 3 > 2
+    with pytest.raises(bsp.BspError, match="INVALID_ARG"):
+        bsp.plan_host(prob, bsp.Capacity(4, 8, 4), [0, 2, 1], [1, 1])                # indptr decreasing
+    with pytest.raises(bsp.BspError, match="INVALID_ARG"):
+        bsp.plan_host(prob, bsp.Capacity(4, 8, 4), [0, 2, 3], [1, 5])                # last_page_len > page
+    with pytest.raises(bsp.BspError, match="INVALID_ARG"):
+        bsp.plan_host(prob, bsp.Capacity(4, 8, 4), [0, 2, 3], [0, 1])                # last_page_len 0
+    pre = bsp.make_problem(bsp.BSP_MODE_PREFILL, 8, 2, 128, 16, True, torch.bfloat16)
+    with pytest.raises(bsp.BspError, match="CAPACITY"):
+        bsp.plan_host(pre, bsp.Capacity(4, 8, 10), [0, 1, 2], [16, 16], qo_indptr=[0, 6, 12])  # 12 > 10 tokens
+    bad = bsp.make_problem(bsp.BSP_MODE_PREFILL, 6, 2, 128, 16, True, torch.bfloat16)   # 128 % 3 != 0
+    with pytest.raises(bsp.BspError, match="128 %"):
+        bsp.plan_host(bad, bsp.Capacity(4, 8, 10), [0, 1], [16], qo_indptr=[0, 6])
+
+
+def test_partials_within_eq13_bound(bsp):
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        B = int(rng.integers(1, 30))
+        C = int(rng.integers(1, 64))
+        kv = rng.integers(1, 20000, size=B)
+        info, *_ = run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(B, int), kv, 16, 32, 8, False, C)
+        assert info.num_partials <= 2 * C <= info.cap_partials
+        assert info.num_items <= info.cap_items and info.num_merges <= info.cap_merges
