@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse paged attention path on GB300.
+
+Step = plan() on the host + the attention kernel + the merge of split
+outputs, over the Llama-3-8B-shaped batched paged decode (64 requests, KV
+lengths U{512..8192}, page size 16, pages permuted over the pool, 32 qo / 8 kv
+heads, head_dim 128, bf16), inputs resident in HBM. value = algorithmic bytes
+of the step (KV + Q + O + LSE + page table) / step time, in GB/s.
+
+Also reported: the attention kernel's roofline against the measured HBM
+copy bandwidth, the same metric end to end through the public API with host
+buffers (host->device copies of every input and device->host copy of O and
+LSE inside the timed region), the oracle on the host cores, the SM clocks
+sampled during the timed region, and secondary workloads (page-size-1 decode
+permuted vs contiguous, ragged causal prefill TFLOP/s, shared-prefix decode).
+
+Multi-GPU: one process per GPU under torch.distributed.run; every rank runs
+its own replica of the workload (the path shards by request, no data-path
+collective), timing is max over ranks and value sums all ranks' bytes.
+`--impl reference` times the oracle (the plain fp64 CPU implementation) as
+the reference arm, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged-KV decode GB/s & ragged prefill TFLOPS, % of GB300 roofline (1 GPU)"
+WORKLOAD = "batched_decode_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only; the data path has no collective)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, clocks, profile summaries
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        try:
+            rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+            os.unlink(self.path)
+        except OSError:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_paged_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(key: str, digest: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[key]
+        if e.get("source_digest") == digest:
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def esize(batch) -> int:
+    return 2 if batch.dtype == "bf16" else 4
+
+
+def decode_bytes(batch) -> int:
+    """Bytes a decode step must move at least once: K and V of every visible
+    token of every kv head, Q, O, LSE and the page table."""
+    e = esize(batch)
+    kv = int(batch.kv_lens.sum()) * batch.num_kv_heads * batch.head_dim * e * 2
+    n_tok = int(batch.qo_indptr[-1])
+    qo = 2 * n_tok * batch.num_qo_heads * batch.head_dim * e
+    lse = n_tok * batch.num_qo_heads * 4
+    meta = 4 * (len(batch.kv_indices) + 2 * (batch.batch + 1) + batch.batch)
+    return kv + qo + lse + meta
+
+
+def prefill_flops(batch) -> float:
+    """4 * D per visible (query, key) pair and qo head (QK^T and PV)."""
+    tot = 0
+    for q, k in zip(batch.qo_lens, batch.kv_lens):
+        q, k = int(q), int(k)
+        if batch.causal:
+            vis = sum(max(0, min(k, i + k - q + 1)) for i in range(q))
+        else:
+            vis = q * k
+        tot += vis
+    return 4.0 * batch.head_dim * batch.num_qo_heads * tot
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def to_dev(batch, dev):
+    return (batch.q.to(dev), batch.k_pages.to(dev), batch.v_pages.to(dev),
+            torch.from_numpy(np.ascontiguousarray(batch.kv_indices, np.int32)).to(dev))
+
+
+def time_kernel_only(pa, batch, dev_t, steps, warmup, qo=None):
+    """Mean attention-kernel and merge-kernel time (ms) over `steps` runs of a fixed plan."""
+    q, k, v, idx = dev_t
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    pa.plan(batch.kv_indptr, batch.last_page_len, qo_indptr=qo)
+    for _ in range(warmup):
+        pa.run_stages(q, k, v, idx, batch.sm_scale, out, lse)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        pa.run_stages(q, k, v, idx, batch.sm_scale, out, lse, events=ev[i])
+    torch.cuda.synchronize()
+    attn = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    merge = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    return attn, merge, out, lse
+
+
+def run_ours(args, rank, world, local):
+    import workloads
+    from block_sparse_paged_gb300 import build
+    build.build()
+    import block_sparse_paged_gb300 as bsp
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    batch = workloads.batched_decode_bf16()
+    nbytes = decode_bytes(batch)
+    q, k, v, idx = to_dev(batch, dev)
+    num_ctas = args.num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, local)
+    pa = bsp.PagedAttention("decode", batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
+                            False, torch.bfloat16, max_batch=batch.batch, num_ctas=num_ctas, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    K, W = args.steps, args.warmup
+
+    def step(events=None):
+        pa.plan(batch.kv_indptr, batch.last_page_len)
+        pa.run_stages(q, k, v, idx, batch.sm_scale, out, lse, events=events)
+
+    for _ in range(W):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(K):
+        step(ev[i])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = max_over_ranks(t0.elapsed_time(t1) / K, world)
+    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    total_bytes = sum_over_ranks(float(nbytes), world)
+    value = total_bytes / (step_ms * 1e-3) / 1e9
+
+    pk, pk_src = peaks()
+    achieved = nbytes / (attn_ms * 1e-3) / 1e9
+    digest = kernel_digest("decode.cu", "device_common.cuh")
+    roofline = {"bound": "hbm", "kernel": "decode_bf16_kernel<128>", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "peak_source": f"{pk_src} (STREAM-style copy)",
+                "traffic": profile_traffic("decode_bf16_batched", digest),
+                "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(attn_ms, 5)}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(bsp, batch, pa, K, W, dev, nbytes, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) values, numpy PCG64)",
+        "config": {"workload": "batched paged decode, Llama-3-8B layer shape: 64 requests x 1 query, KV U{512..8192}, "
+                               "page 16 (permuted pool), 32 qo / 8 kv heads, head_dim 128",
+                   "name": WORKLOAD, "global_batch": batch.batch * world, "kv_tokens": int(batch.kv_lens.sum()),
+                   "num_ctas": num_ctas, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 1.14 GB of KV per step vs 129 MB L2, no flush",
+                   "step": "plan (host) + attention kernel + merge-of-partials kernel",
+                   "algorithmic_bytes_per_step": nbytes, "merge_ms": round(merge_ms, 5)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(batch, args.cpu_seconds)
+    if rank == 0 and not args.no_secondary:
+        del q, k, v, idx, out, lse
+        torch.cuda.empty_cache()
+        result["secondary"] = secondary(bsp, dev, args, pk)
+    return result
+
+
+def run_e2e(bsp, batch, pa, K, W, dev, nbytes, world):
+    """Same metric through the public API, inputs copied host -> device from
+    pinned memory and O, LSE copied back, every step."""
+    hq = batch.q.pin_memory()
+    hk = batch.k_pages.pin_memory()
+    hv = batch.v_pages.pin_memory()
+    hidx = torch.from_numpy(np.ascontiguousarray(batch.kv_indices, np.int32)).pin_memory()
+    dq = torch.empty_like(hq, device=dev)
+    dk = torch.empty_like(hk, device=dev)
+    dv = torch.empty_like(hv, device=dev)
+    didx = torch.empty_like(hidx, device=dev)
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty(hq.shape[:2], dtype=torch.float32).pin_memory()
+
+    def step():
+        pa.plan(batch.kv_indptr, batch.last_page_len)
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        out, lse = pa.run(dq, dk, dv, didx, batch.sm_scale)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    n = max(1, min(K, 10))
+    for _ in range(max(1, min(W, 3))):
+        step()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(n):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1) / n, world)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hidx.numel() * 4 + pa.info.metadata_bytes
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    total = sum_over_ranks(float(nbytes), world)
+    return {"value": round(total / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "KV pool, Q and page table copied from pinned host memory every step"}
+
+
+def cpu_baseline(batch, seconds: float):
+    """The oracle, as it stands, on all host cores over the full workload,
+    repeated for about `seconds`."""
+    import oracle
+    k32 = batch.k_pages.float().numpy()
+    v32 = batch.v_pages.float().numpy()
+    n_tok = int(batch.qo_indptr[-1])
+    tok = np.repeat(np.arange(n_tok, dtype=np.int64), batch.num_qo_heads)
+    head = np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), n_tok)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_rows_of(batch, tok, head, k_f32=k32, v_f32=v32)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    gbs = decode_bytes(batch) * reps / el / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.num_threads_available(), "kind": "oracle",
+            "sample": f"full workload (64 requests x 32 heads), {reps} repetitions in {el:.1f} s, fp64"}
+
+
+def secondary(bsp, dev, args, pk):
+    import workloads
+    res = {}
+    steps = max(5, min(args.steps, 50))
+    warm = max(3, args.warmup)
+    # page size 1, permuted vs contiguous
+    perm, cont = workloads.vector_sparse_decode_bf16()
+    r = {}
+    for tag, b in (("permuted", perm), ("contiguous", cont)):
+        C = args.num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
+        pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, 1, False, torch.bfloat16,
+                                max_batch=b.batch, num_ctas=C, device=dev)
+        attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm)
+        gbs = decode_bytes(b) / ((attn + merge) * 1e-3) / 1e9
+        r[tag] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "attn_ms": round(attn, 4),
+                  "merge_ms": round(merge, 4)}
+        del pa
+        torch.cuda.empty_cache()
+    r["permuted_over_contiguous"] = round(r["permuted"]["GB/s"] / r["contiguous"]["GB/s"], 4)
+    r["workload"] = "32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16"
+    res["vector_sparse_decode"] = r
+    del perm, cont
+    # ragged causal prefill
+    b = workloads.ragged_causal_prefill_bf16()
+    try:
+        pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
+                                torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+        attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
+        fl = prefill_flops(b)
+        tf = fl / ((attn + merge) * 1e-3) / 1e12
+        res["ragged_causal_prefill"] = {"TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                                        "flops": fl, "attn_ms": round(attn, 4), "merge_ms": round(merge, 4)}
+    except Exception as e:  # the prefill kernel may not be built for this shape
+        res["ragged_causal_prefill"] = {"unavailable": str(e)[:200]}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    import oracle
+    import workloads
+    if rank != 0:
+        return None
+    oracle.build()
+    batch = workloads.batched_decode_bf16()
+    k32 = batch.k_pages.float().numpy()
+    v32 = batch.v_pages.float().numpy()
+    # each step: the first 16 requests, all 32 heads (a bounded sample of the workload)
+    nreq = 16
+    tok = np.repeat(np.arange(nreq, dtype=np.int64), batch.num_qo_heads)
+    head = np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), nreq)
+    sub = workloads.scaled(batch, qo_indptr=batch.qo_indptr[:nreq + 1], kv_indptr=batch.kv_indptr[:nreq + 1],
+                           last_page_len=batch.last_page_len[:nreq])
+    nbytes = decode_bytes(sub)
+    for _ in range(args.warmup):
+        oracle.attention_rows_of(batch, tok, head, k_f32=k32, v_f32=v32)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_rows_of(batch, tok, head, k_f32=k32, v_f32=v32)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = nbytes / (ms * 1e-3) / 1e9
+    cores = oracle.num_threads_available()
+    return {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) values, numpy PCG64)",
+            "config": {"workload": "batched paged decode, Llama-3-8B layer shape (first 16 of the 64 requests per step)",
+                       "name": WORKLOAD, "sample_requests": nreq},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {nreq} requests x 32 heads per step, fp64 C oracle"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--num-ctas", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -175,6 +175,31 @@ class PagedAttention:
                 N.check(self.lib.bsp_prefill_run(*args, k_pages.shape[0], *tail, s))
         return (out, lse) if return_lse else out
 
+    def run_stages(self, q, k_pages, v_pages, kv_indices, sm_scale, out, lse, stream=None, events=None):
+        """The run as its two launches (attention kernel, merge of partials) on
+        `stream`; `events` = (e0, e1, e2) are recorded before, between and after
+        them when given. out and lse must be preallocated."""
+        dev = self.device
+        with torch.cuda.device(dev):
+            st = stream if stream is not None else torch.cuda.current_stream()
+            s = ctypes.c_void_p(st.cuda_stream)
+            ws = ctypes.c_void_p(self.workspace.data_ptr())
+            o_p = _dev(out, "out", self.dtype, dev)
+            l_p = None if lse is None else _dev(lse, "lse", torch.float32, dev)
+            if events:
+                events[0].record(st)
+            N.check(self.lib.bsp_run_attention(ctypes.byref(self.info), _dev(q, "q", self.dtype, dev),
+                                               _dev(k_pages, "k_pages", self.dtype, dev),
+                                               _dev(v_pages, "v_pages", self.dtype, dev),
+                                               _dev(kv_indices, "kv_indices", torch.int32, dev), k_pages.shape[0],
+                                               ctypes.c_float(sm_scale), o_p, l_p, ws, s))
+            if events:
+                events[1].record(st)
+            N.check(self.lib.bsp_run_merge_partials(ctypes.byref(self.info), o_p, l_p, ws, s))
+            if events:
+                events[2].record(st)
+        return out, lse
+
     def check_device_error(self, stream=None) -> int:
         word = ctypes.c_int32()
         with torch.cuda.device(self.device):

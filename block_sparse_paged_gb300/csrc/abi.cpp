@@ -86,6 +86,31 @@ extern "C" int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const v
     return launch_reduce(plan, o, lse, workspace, stream);
 }
 
+extern "C" int bsp_run_attention(const bsp_plan_info *plan, const void *q, const void *k_pages,
+                                 const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
+                                 float sm_scale, void *o, float *lse, void *workspace, bsp_stream_t stream) {
+    clear_error();
+    if (!plan) return fail(BSP_ERR_INVALID_ARG, "plan is NULL");
+    const int mode = plan->problem.mode;
+    int rc = check_plan(plan, mode, workspace);
+    if (rc != BSP_OK) return rc;
+    if (!q || !k_pages || !v_pages || !kv_indices || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (mode == BSP_MODE_DECODE)
+        return launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, workspace, stream);
+    if (num_pages < 1) return fail(BSP_ERR_INVALID_ARG, "num_pages must be positive");
+    return launch_prefill(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
+}
+
+extern "C" int bsp_run_merge_partials(const bsp_plan_info *plan, void *o, float *lse, void *workspace,
+                                      bsp_stream_t stream) {
+    clear_error();
+    if (!plan) return fail(BSP_ERR_INVALID_ARG, "plan is NULL");
+    int rc = check_plan(plan, plan->problem.mode, workspace);
+    if (rc != BSP_OK) return rc;
+    if (!o) return fail(BSP_ERR_INVALID_ARG, "o is NULL");
+    return launch_reduce(plan, o, lse, workspace, stream);
+}
+
 extern "C" int bsp_merge_state(const void *o_a, const float *lse_a, const void *o_b, const float *lse_b, void *o_out,
                                float *lse_out, int64_t n_rows, int32_t num_heads, int32_t head_dim, int32_t dtype,
                                bsp_stream_t stream) {

@@ -235,6 +235,24 @@ int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_page
                     float sm_scale, void *o, float *lse, void *workspace, bsp_stream_t stream);
 
 /*
+ * The two stages of a run, for callers that time or schedule them apart
+ * (bsp_decode_run / bsp_prefill_run are exactly these two calls in order):
+ *   bsp_run_attention       the attention kernel over the plan's work items
+ *                           (final outputs for unsplit tiles, partial states in
+ *                           the workspace for split ones); num_pages is used by
+ *                           prefill and ignored by decode
+ *   bsp_run_merge_partials  the merge of partial states over the reduction map
+ *                           (engineering walkthrough §VIII.4, the contraction
+ *                           kernel); it always launches, with a fixed grid, and
+ *                           does nothing when the plan split no output.
+ */
+int bsp_run_attention(const bsp_plan_info *plan, const void *q, const void *k_pages,
+                      const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
+                      float sm_scale, void *o, float *lse, void *workspace, bsp_stream_t stream);
+int bsp_run_merge_partials(const bsp_plan_info *plan, void *o, float *lse, void *workspace,
+                           bsp_stream_t stream);
+
+/*
  * Merge two sets of attention states (technical review §3.2 eq 6 and §3.3
  * Algorithm 1): with m = max(LSE_a, LSE_b), a = e^(LSE_a - m), b = e^(LSE_b - m),
  *   O = (a O_a + b O_b) / (a + b),   LSE = m + log(a + b);

@@ -1,0 +1,192 @@
+"""Decode path on the GPU through the C ABI, element by element against the
+oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import (compare, lib, oracle_full, run_batch, sample_rows, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    return lib()
+
+
+def test_tiny_decode_f32(bsp):
+    """3 requests, KV 10/3/7, page 4, 16-page permuted pool with NaN in unused
+    pages and page tails, 4/2 heads, head_dim 64, fp32, sm_scale 1/8."""
+    b = workloads.tiny_decode_f32()
+    O, L = oracle_full(b)
+    for C in (1, 3, 64):
+        out, lse, _ = run_batch(bsp, b, num_ctas=C)
+        compare(out, lse, O, L, "f32")
+
+
+CASES = [
+    # (seed, kv lens, H_qo, H_kv, D, page, num_ctas)
+    (1, [1, 64, 65, 127, 200, 0, 3000], 32, 8, 128, 16, 7),
+    (2, [5, 17, 64, 1000, 4097], 8, 8, 128, 1, 5),
+    (3, [33, 300, 2, 511, 1500, 64], 16, 2, 128, 3, 11),
+    (4, [700, 1, 129, 4000], 16, 1, 128, 16, 3),
+    (5, [100, 257, 0, 63], 4, 2, 64, 4, 6),
+    (6, [2048, 1024, 17], 32, 4, 64, 1, 400),
+    (7, [12345, 5, 999], 32, 8, 128, 32, 2),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
+def test_random_bf16_decode(bsp, case):
+    seed, kv, hq, hk, D, ps, C = case
+    b = workloads.paged_batch(seed, np.ones(len(kv), int), kv, hq, hk, D, ps, "bf16", extra_pages=3)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=C)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_batched_decode_full_size(bsp):
+    """Llama-3-8B-shaped batch at full size (64 requests, KV U{512..8192}, page
+    16), sampled rows against the oracle, with the bench's CTA count."""
+    b = workloads.batched_decode_bf16()
+    out, lse, pa = run_batch(bsp, b)
+    tok, head = sample_rows(b, 256, 11)
+    O, L = oracle.attention_rows_of(b, tok, head)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    # run twice: bitwise identical (fixed plan, fixed reduction order)
+    q, k, v, idx = to_dev(b)
+    out2, lse2 = pa.run(q, k, v, idx, b.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_vector_sparse_permuted_equals_contiguous(bsp):
+    """Page size 1, every slot permuted, 64/8 heads: the permuted and the
+    contiguous layouts give bitwise-equal outputs; sampled rows match the oracle."""
+    perm, cont = workloads.vector_sparse_decode_bf16()
+    out_p, lse_p, _ = run_batch(bsp, perm)
+    out_c, lse_c, _ = run_batch(bsp, cont)
+    assert torch.equal(out_p, out_c) and torch.equal(lse_p, lse_c)
+    tok, head = sample_rows(perm, 128, 12)
+    O, L = oracle.attention_rows_of(perm, tok, head)
+    compare(out_p, lse_p, O, L, "bf16", rows=(tok, head))
+
+
+def test_shared_prefix_full_view_decode(bsp):
+    """The shared-prefix batch read without composition (every request over
+    prefix + suffix pages), including the 32768-token outlier; sampled rows."""
+    sp = workloads.shared_prefix_decode_bf16()
+    out, lse, _ = run_batch(bsp, sp.full)
+    tok, head = sample_rows(sp.full, 128, 13)
+    O, L = oracle.attention_rows_of(sp.full, tok, head)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))
+
+
+def test_cuda_graph_replay_with_new_plan(bsp):
+    """Capture one run, then re-plan with other lengths into the same workspace
+    and replay: the replay equals an eager run of the new plan."""
+    hq, hk, D, ps = 32, 8, 128, 16
+    a = workloads.paged_batch(21, np.ones(6, int), [100, 2000, 5, 700, 64, 3000], hq, hk, D, ps, "bf16", extra_pages=40)
+    bb = workloads.paged_batch(22, np.ones(6, int), [3000, 1, 64, 65, 2500, 10], hq, hk, D, ps, "bf16", extra_pages=40)
+    pa = bsp.PagedAttention("decode", hq, hk, D, ps, False, torch.bfloat16, max_batch=6, num_ctas=24)
+    pool = max(a.k_pages.shape[0], bb.k_pages.shape[0])
+    q = torch.empty_like(a.q, device="cuda")
+    k = torch.empty((pool,) + tuple(a.k_pages.shape[1:]), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    idx = torch.zeros(8192, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+
+    def load(batch):
+        q.copy_(batch.q)
+        k[: batch.k_pages.shape[0]].copy_(batch.k_pages)
+        v[: batch.v_pages.shape[0]].copy_(batch.v_pages)
+        idx[: len(batch.kv_indices)].copy_(torch.from_numpy(batch.kv_indices))
+
+    load(a)
+    pa.plan(a.kv_indptr, a.last_page_len)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.run(q, k, v, idx, a.sm_scale, out=out, lse=lse)  # warm up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.run(q, k, v, idx, a.sm_scale, out=out, lse=lse)
+    g.replay()
+    torch.cuda.synchronize()
+    O, L = oracle_full(a)
+    compare(out, lse, O, L, "bf16")
+    load(bb)
+    pa.plan(bb.kv_indptr, bb.last_page_len)
+    g.replay()
+    torch.cuda.synchronize()
+    O, L = oracle_full(bb)
+    compare(out, lse, O, L, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_merge_state_of_split_attention(bsp, dtype):
+    """Two attention states over disjoint page ranges of the same requests,
+    merged on the GPU, equal attention over all pages (oracle)."""
+    b = workloads.paged_batch(30, np.ones(8, int), [40, 33, 100, 17, 64, 250, 9, 128], 16, 4, 128, 4, dtype,
+                              extra_pages=5)
+    half = [(int(b.kv_indptr[i]) + int(b.kv_indptr[i + 1])) // 2 for i in range(b.batch)]
+    first = workloads.scaled(b, kv_indptr=np.array([0] + [h - int(b.kv_indptr[i]) for i, h in enumerate(half)]).cumsum().astype(np.int32),
+                             kv_indices=np.concatenate([b.kv_indices[b.kv_indptr[i]:half[i]] for i in range(b.batch)]).astype(np.int32),
+                             last_page_len=np.full(b.batch, b.page_size, np.int32))
+    second = workloads.scaled(b, kv_indptr=np.array([0] + [int(b.kv_indptr[i + 1]) - h for i, h in enumerate(half)]).cumsum().astype(np.int32),
+                              kv_indices=np.concatenate([b.kv_indices[half[i]:b.kv_indptr[i + 1]] for i in range(b.batch)]).astype(np.int32))
+    O1, L1 = oracle_full(first)
+    O2, L2 = oracle_full(second)
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    out, lse = bsp.merge_state(torch.from_numpy(O1).to(t).cuda(), torch.from_numpy(L1).float().cuda(),
+                               torch.from_numpy(O2).to(t).cuda(), torch.from_numpy(L2).float().cuda())
+    torch.cuda.synchronize()
+    O, L = oracle_full(b)
+    compare(out, lse, O, L, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_merge_state_arbitrary_states(bsp, dtype):
+    """Arbitrary states with empty ones (LSE = -inf) on either or both sides;
+    in-place use into the first operand."""
+    rng = np.random.default_rng(31)
+    n, H, D = 333, 8, 128
+    oa = rng.standard_normal((n, H, D)).astype(np.float32)
+    ob = rng.standard_normal((n, H, D)).astype(np.float32)
+    la = (rng.standard_normal((n, H)) * 4).astype(np.float32)
+    lb = (rng.standard_normal((n, H)) * 4).astype(np.float32)
+    la[::7, 0] = -np.inf
+    lb[::5, 1] = -np.inf
+    la[3, :] = lb[3, :] = -np.inf
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    ta, tb = torch.from_numpy(oa).to(t), torch.from_numpy(ob).to(t)
+    Oe, Le = oracle.merge_states(ta.float().numpy(), la, tb.float().numpy(), lb)
+    out, lse = bsp.merge_state(ta.cuda(), torch.from_numpy(la).cuda(), tb.cuda(), torch.from_numpy(lb).cuda())
+    torch.cuda.synchronize()
+    compare(out, lse, Oe, Le, dtype, rounding_aware=True)
+    # a pass-through side is copied bit for bit
+    pa_rows = np.isneginf(lb) & ~np.isneginf(la)
+    assert torch.equal(out.cpu()[torch.from_numpy(pa_rows)], ta[torch.from_numpy(pa_rows)])
+    # in place into a
+    a_dev, la_dev = ta.cuda(), torch.from_numpy(la).cuda()
+    bsp.merge_state(a_dev, la_dev, tb.cuda(), torch.from_numpy(lb).cuda(), out=a_dev, lse_out=la_dev)
+    torch.cuda.synchronize()
+    assert torch.equal(a_dev, out) and torch.equal(la_dev, lse)
+
+
+def test_run_rejects_bad_arguments(bsp):
+    b = workloads.paged_batch(41, [1, 1], [10, 20], 8, 2, 128, 4, "bf16")
+    pa = bsp.PagedAttention("decode", 8, 2, 128, 4, False, torch.bfloat16, max_batch=2, num_ctas=4)
+    with pytest.raises(RuntimeError):
+        pa.run(*to_dev(b), b.sm_scale)       # no plan yet
+    pa.plan(b.kv_indptr, b.last_page_len)
+    q, k, v, idx = to_dev(b)
+    with pytest.raises(ValueError):
+        pa.run(q.float(), k, v, idx)         # wrong dtype
+    with pytest.raises(ValueError):
+        pa.run(q[:, :4], k, v, idx)          # wrong head count
