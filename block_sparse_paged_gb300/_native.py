@@ -24,13 +24,14 @@ BSP_DTYPE_BF16 = 0
 BSP_DTYPE_F32 = 1
 BSP_MODE_DECODE = 0
 BSP_MODE_PREFILL = 1
+BSP_STATIC_WORKSPACE_BYTES = 8 << 20
 
 _ERR_NAMES = {BSP_ERR_INVALID_ARG: "INVALID_ARG", BSP_ERR_CAPACITY: "CAPACITY", BSP_ERR_CUDA: "CUDA",
               BSP_ERR_UNSUPPORTED: "UNSUPPORTED", BSP_ERR_DEVICE_CHECK: "DEVICE_CHECK"}
 
 EXPORTED = ["bsp_default_num_ctas", "bsp_workspace_size", "bsp_host_staging_size", "bsp_plan",
             "bsp_decode_run", "bsp_prefill_run", "bsp_run_attention", "bsp_run_merge_partials",
-            "bsp_merge_state", "bsp_check_device_error",
+            "bsp_merge_state", "bsp_decode_run_static", "bsp_check_device_error",
             "bsp_last_error", "bsp_version"]
 
 
@@ -97,6 +98,7 @@ def load():
         "bsp_run_attention": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_run_merge_partials": ([PI, vp, vp, vp, vp], ctypes.c_int),
         "bsp_merge_state": ([vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp], ctypes.c_int),
+        "bsp_decode_run_static": ([PI, vp, vp, vp, vp, vp, f32, vp, vp, vp], ctypes.c_int),
         "bsp_check_device_error": ([PI, vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "bsp_last_error": ([], ctypes.c_char_p),
         "bsp_version": ([], ctypes.c_char_p),

@@ -267,6 +267,39 @@ int bsp_merge_state(const void *o_a, const float *lse_a, const void *o_b, const 
                     void *o_out, float *lse_out, int64_t n_rows, int32_t num_heads,
                     int32_t head_dim, int32_t dtype, bsp_stream_t stream);
 
+/*
+ * Decode run without any device allocation by the caller or the library.
+ *
+ * No counterpart on the pages: this is a convenience of this library. It is
+ * for callers that cannot call cudaMalloc where they run attention, such as a
+ * host framework that has handed all device memory to its own pool and
+ * forbids allocation while serving, or code running inside a stream capture
+ * in global mode. The caller plans as usual (bsp_plan, where `workspace` may
+ * be NULL for a host-only plan) and passes the plan and its staging image;
+ * this call copies the plan into a fixed device array owned by the library,
+ * uses that array as the workspace (plan metadata and partial states), runs
+ * the decode kernel and the merge of partials, and allocates nothing.
+ *
+ *   plan          from bsp_plan, mode BSP_MODE_DECODE; its workspace_bytes
+ *                 must not exceed BSP_STATIC_WORKSPACE_BYTES (else
+ *                 BSP_ERR_CAPACITY: lower capacity.num_ctas or max_batch)
+ *   host_staging  the staging buffer that bsp_plan wrote this plan into
+ *   other arguments as in bsp_decode_run (device pointers, caller-owned).
+ *
+ * The array (BSP_STATIC_WORKSPACE_BYTES of device memory) exists once per
+ * device in every process that loads the library and lives until the
+ * process exits. The first call on a device looks its address up
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps the previous
+ * call's contents: calls whose work may overlap on the GPU (two streams, or
+ * two host threads) race on it and must be serialised by the caller, e.g.
+ * by using one stream.
+ */
+#define BSP_STATIC_WORKSPACE_BYTES (8u << 20)
+int bsp_decode_run_static(const bsp_plan_info *plan, const void *host_staging, const void *q,
+                          const void *k_pages, const void *v_pages, const int32_t *kv_indices,
+                          float sm_scale, void *o, float *lse, bsp_stream_t stream);
+
 /* Read (and clear) the device error word that kernels set when a bounded wait
  * gives up or a bounds check trips (it lives in the workspace section at
  * plan->off_status). Synchronises `stream`. *word_out = 0 when clean;
