@@ -6,54 +6,69 @@
 // every byte of K and V is read once, and the g heads that share a kv head reuse
 // each loaded KV tile (head-group fusion, technical review eq 3; overview ⑦).
 //
-// bf16 kernel (one persistent CTA of 4 warps per plan queue):
-//   - loader: page-indexed 16-byte cp.async of K and V rows into a 3-stage
-//     shared-memory ring (sparse gather, dense compute: overview ⑥,
-//     walkthrough §IV.2 and §V.4). Stage = 64 tokens; the ring runs across the
-//     CTA's work items, so the next item's first tiles load while the current
-//     one finishes. Each thread loads one token per stage and prefetches the
-//     page index of its next token one stage early.
-//   - compute: each warp takes 16 of the 64 tokens; S = Q K^T and O += P V on
-//     the warp-level tensor-core MMA (m16n8k16, rows = the g fused heads), fp32
-//     online softmax in base 2 with the scale folded into log2(e)
-//     (walkthrough §II.2), then the four warps' states are merged in shared
-//     memory at the end of each item.
+// bf16 kernel (one persistent CTA per plan queue, one CTA per SM):
+//   - loaders (warp 4: K, warp 5: V): 16-byte cp.async copies addressed
+//     through the page table, each warp instruction covering two whole
+//     256-byte rows; each lane computes two row offsets per stage
+//     (sparse gather, dense compute: overview ⑥, walkthrough §IV.2 and §V.4),
+//     into a 5-stage ring of 64-token stages with padded rows; page indices
+//     are fetched one stage ahead and shared by shuffles. mbarriers carry the
+//     handshake (full: every producer lane's copies landed, through
+//     cp.async.mbarrier.arrive; empty: the four compute warps are done with
+//     the stage), and the ring runs across the CTA's work items, so the next
+//     item's first stages load while the current one finishes.
+//   - compute (warps 0..3): each warp takes 16 of the 64 tokens; S = Q K^T and
+//     O += P V on the warp-level tensor-core MMA (m16n8k16, rows = the g fused
+//     heads), fp32 online softmax in base 2 with the scale folded into
+//     log2(e) (walkthrough §II.2); at the end of each item the four warps'
+//     states are merged in shared memory.
 //   - output: the final (O, LSE) when the item is its output's only chunk,
 //     else an fp32 partial state in the workspace slot the plan assigned
 //     (overview ⑨, write-through of unsplit requests).
+//   - every wait is bounded (about 1 s of polls); a wait that gives up sets the workspace
+//     status word and an abort flag the other warps see, and the CTA returns.
 // Reduction kernel: the reduction map's slots of each split output, merged in
 // ascending order with a common maximum (technical review eq 6), no atomics.
 #include <cfloat>
 
 #include "bsp_internal.h"
 #include "device_common.cuh"
+#include "sm100.cuh"
 
 namespace bsp {
 namespace {
 
 using namespace dev;
 
-constexpr int kDecThreads = 128;
+constexpr int kDecThreads = 128;            // fp32 kernel
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kTileK = 64;      // KV tokens per ring stage
-constexpr int kStages = 3;
-constexpr int kMmaRows = 16;    // fused heads per tile (M of the MMA)
+constexpr int kMmaRows = 16;                 // fused heads per tile (M of the MMA)
+
+// bf16 kernel: warps 0..3 compute, warps 4 and 5 load K and V.
+constexpr int kConsumers = 4;
+constexpr int kWsThreads = 32 * (kConsumers + 2);
+constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per consumer warp)
+constexpr int kStages = 5;
+constexpr uint32_t kWaitHintNs = 100000;     // one poll sleeps up to 100 us unless the phase completes
+constexpr uint32_t kWaitPolls = 10000;       // so a wait gives up after about 1 s: a fault, not a stall
 
 template <int D>
 struct DecodeLayout {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kChunks = D / 8;                 // 16-byte chunks per row
-    static constexpr int kTileBytes = kTileK * kRowBytes; // K (or V) part of a stage
+    static constexpr int kPitch = D * 2 + 16;              // padded row: ldmatrix phases hit 8 bank groups
+    static constexpr int kTileBytes = kTileK * kPitch;     // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStatBytes = kDecWarps * kMmaRows * 2 * sizeof(float);
-    static constexpr int kSmemBytes = kStages * kStageBytes + kStatBytes;
-    // The merge scratch of one item reuses a free stage: 4 warps x 16 rows x D floats.
-    static_assert(kDecWarps * kMmaRows * D * 4 <= kStageBytes, "merge scratch must fit in one stage");
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kScratchBytes = kConsumers * kMmaRows * D * 4;   // per-warp O rows for the item merge
+    static constexpr int kStatBytes = kConsumers * kMmaRows * 2 * 4;      // per-warp (m, l)
+    static constexpr int kBarOff = kRingBytes + kScratchBytes + kStatBytes;
+    static constexpr int kNumBars = 2 * kStages + 2;        // full[S], empty[S], merge_in, merge_out
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
 };
 
 struct DecodeParams {
     const uint8_t *ws;
-    uint64_t off_queue, off_items, off_plse, off_po;
+    uint64_t off_queue, off_items, off_plse, off_po, off_status;
     const void *q, *k, *v;
     const int32_t *kv_indices;
     void *o;
@@ -62,85 +77,121 @@ struct DecodeParams {
     int H_qo, H_kv, g, page_size, tile_rows;
 };
 
-// Swizzled byte offset of 16-byte chunk c of row r inside a K or V tile:
-// chunks are XOR-permuted by the row's low 3 bits, so the 8 rows an ldmatrix
-// phase reads fall in 8 different bank groups.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)(r * DecodeLayout<D>::kRowBytes + ((c ^ (r & 7)) << 4));
+// Status codes the decode kernel writes to the workspace status word.
+constexpr int kStatusProducerWait = 0x101;
+constexpr int kStatusConsumerWait = 0x102;
+constexpr int kStatusMergeWait = 0x103;
+
+// Bounded mbarrier wait that also gives up as soon as another warp aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
+                                              int code) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (sm100::mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    atomicCAS(status, 0, code);
+    return false;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const DecodeParams p) {
     using LY = DecodeLayout<D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
+    int *status = reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + p.off_status);
     const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
-    const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
     const uint32_t sbase = smem_u32(smem);
+    const uint32_t full0 = sbase + LY::kBarOff, empty0 = full0 + kStages * 8;
+    const uint32_t merge_in = empty0 + kStages * 8, merge_out = merge_in + 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + LY::kBarOff + LY::kNumBars * 8);
 
-    // ---------------- producer: walks (item, tile) in queue order ----------
-    const int ptok = tid >> 1, phalf = tid & 1;
-    int pi = it0 - 1, pt = 0, pn = 0;             // item, tile within item, tiles of item
-    int p_head = 0, p_start = 0, p_end = 0, p_base = 0;
-    bool p_has = false, p_valid = false;
-    int p_page = 0, p_off = 0;                      // prefetched address of this thread's token
+    // Rows past a chunk's end are never copied: zero the ring once so that
+    // they hold finite values (their probabilities are exactly 0).
+    for (int i = tid; i < LY::kRingBytes / 16; i += kWsThreads) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    sm100::fence_proxy_async_smem();
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            sm100::mbar_init(full0 + 8 * s, 64);          // one no-increment arrival per producer lane
+            sm100::mbar_init(empty0 + 8 * s, kConsumers);
+        }
+        sm100::mbar_init(merge_in, kConsumers);
+        sm100::mbar_init(merge_out, kConsumers);
+        *abort_flag = 0;
+        sm100::fence_barrier_init();
+    }
+    __syncthreads();
 
-    auto p_advance = [&]() {
-        ++pt;
-        while (pt >= pn) {
-            ++pi;
-            if (pi >= it1) { p_has = false; return; }
-            const bsp_work_item &w = items[pi];
-            p_head = w.kv_head; p_start = w.kv_start; p_end = w.kv_end; p_base = w.page_base;
-            pn = (p_end - p_start + kTileK - 1) / kTileK;
-            pt = 0;
-        }
-        p_has = true;
-        const int t = p_start + pt * kTileK + ptok;
-        p_valid = t < p_end;
-        if (p_valid) {
-            p_page = __ldg(p.kv_indices + p_base + t / p.page_size);
-            p_off = t % p.page_size;
-        }
-    };
-    auto p_issue = [&](int buf) {
-        if (p_has) {
-            const uint32_t dk = sbase + buf * LY::kStageBytes;
-            const uint32_t dv = dk + LY::kTileBytes;
-            const size_t row = p_valid ? ((size_t)p_page * p.page_size + p_off) * p.H_kv + p_head : 0;
-            const __nv_bfloat16 *sk = kg + row * D;
-            const __nv_bfloat16 *sv = vg + row * D;
-            const int nb = p_valid ? 16 : 0;
+    if (warp >= kConsumers) {
+        // ---------------- producers: warp 4 copies K rows, warp 5 V rows ----
+        // Each lane first turns the page ids of tokens `lane` and `lane + 32` of
+        // the stage into byte offsets of their rows (one division each), then
+        // every warp instruction copies T = 32 / C whole rows, C = D / 8 chunks
+        // of 16 bytes per row, taking the row offsets by shuffle.
+        constexpr int C = D / 8, T = 32 / C;
+        const bool is_v = warp == kConsumers + 1;
+        const char *src = static_cast<const char *>(is_v ? p.v : p.k);
+        const uint32_t part = is_v ? LY::kTileBytes : 0;
+        const int my_chunk = lane % C, my_sub = lane / C;
+        int k = 0;
+        for (int it = it0; it < it1 && !*abort_flag; ++it) {
+            const bsp_work_item w = items[it];
+            const int len = w.kv_end - w.kv_start;
+            const int nt = (len + kTileK - 1) / kTileK;
+            int pg[2] = {0, 0};
+            auto fetch = [&](int t, int (&dst)[2]) {
 #pragma unroll
-            for (int i = 0; i < LY::kChunks / 2; ++i) {
-                const int c = phalf * (LY::kChunks / 2) + i;
-                cp_async_16(dk + swz<D>(ptok, c), sk + c * 8, nb);
-                cp_async_16(dv + swz<D>(ptok, c), sv + c * 8, nb);
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = lane + 32 * jj;
+                    const int tok = w.kv_start + t * kTileK + j;
+                    if (t * kTileK + j < len) dst[jj] = __ldg(p.kv_indices + w.page_base + tok / p.page_size);
+                }
+            };
+            if (nt > 0) fetch(0, pg);
+            for (int t = 0; t < nt; ++t, ++k) {
+                // byte offsets of this lane's two rows, then the next tile's page ids
+                uint64_t off[2];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int tok = w.kv_start + t * kTileK + lane + 32 * jj;
+                    off[jj] = (((uint64_t)pg[jj] * p.page_size + tok % p.page_size) * p.H_kv + w.kv_head) * (D * 2);
+                }
+                if (t + 1 < nt) fetch(t + 1, pg);
+                const int s = k % kStages;
+                const bool ok = wait_or_abort(empty0 + 8 * s, ((k / kStages) & 1) ^ 1, abort_flag, status,
+                                              kStatusProducerWait);
+                if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: every lane leaves together
+                const int n = min(kTileK, len - t * kTileK);
+                const uint32_t dst = sbase + s * LY::kStageBytes + part + (uint32_t)my_chunk * 16;
+#pragma unroll
+                for (int i = 0; i < kTileK / T; ++i) {
+                    const int j = i * T + my_sub;                     // token within the stage
+                    const int half = (i * T) >> 5;                    // same for the whole warp: T divides 32
+                    const uint64_t o = __shfl_sync(0xffffffffu, off[half], j & 31);
+                    if (j < n) cp_async_16(dst + j * LY::kPitch, src + o + my_chunk * 16, 16);
+                }
+                // arrive on full[s] once this lane's copies have landed
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(full0 + 8 * s) : "memory");
             }
         }
-        cp_async_commit();
-        p_advance();
-    };
+        asm volatile("cp.async.wait_all;\n" ::: "memory");  // nothing may still be in flight when the CTA exits
+        return;
+    }
 
-    p_advance();
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) p_issue(s);
-
-    // ---------------- consumer ---------------------------------------------
+    // ---------------- consumers: warps 0..3 ----------------------------------
     const int g = p.g;
     const int r0 = lane >> 2, r1 = r0 + 8;
-    float *stats = reinterpret_cast<float *>(smem + kStages * LY::kStageBytes);  // [warp][16][m, l]
-    int j = 0;  // tiles consumed so far (ring position)
+    float *scratch = reinterpret_cast<float *>(smem + LY::kRingBytes);                       // [warp][16][D]
+    float *stats = reinterpret_cast<float *>(smem + LY::kRingBytes + LY::kScratchBytes);   // [warp][16][m, l]
+    int k = 0, merges = 0;
     for (int it = it0; it < it1; ++it) {
         const bsp_work_item w = items[it];
         const int len = w.kv_end - w.kv_start;
-        const int ntiles = (len + kTileK - 1) / kTileK;
+        const int nt = (len + kTileK - 1) / kTileK;
 
         // Q fragments of the g fused rows (rows >= g are zero)
         uint32_t qa[D / 16][4];
@@ -163,26 +214,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-        for (int t = 0; t < ntiles; ++t, ++j) {
-            p_issue((j + kStages - 1) % kStages);
-            cp_async_wait<kStages - 1>();
-            __syncthreads();
+        for (int t = 0; t < nt; ++t, ++k) {
+            const int s = k % kStages;
+            const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
+            if (!__all_sync(0xffffffffu, ok)) return;
             const int valid = min(kTileK, len - t * kTileK) - warp * 16;  // this warp's tokens
             if (valid > 0) {
-                const uint32_t kb = sbase + (j % kStages) * LY::kStageBytes;
+                const uint32_t kb = sbase + s * LY::kStageBytes;
                 const uint32_t vb = kb + LY::kTileBytes;
-                float s[2][4];
+                float sc[2][4];
 #pragma unroll
-                for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+                for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
                 {
                     const int mi = lane >> 3;
-                    const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+                    const uint32_t rowaddr = kb + (uint32_t)(warp * 16 + (mi >> 1) * 8 + (lane & 7)) * LY::kPitch +
+                                             (uint32_t)(mi & 1) * 16;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + swz<D>(row, kk * 2 + (mi & 1)), b0, b1, b2, b3);
-                        mma_bf16_16816(s[0], qa[kk], b0, b1);
-                        mma_bf16_16816(s[1], qa[kk], b2, b3);
+                        ldmatrix_x4(rowaddr + kk * 32, b0, b1, b2, b3);
+                        mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                        mma_bf16_16816(sc[1], qa[kk], b2, b3);
                     }
                 }
                 // scale into base 2, mask tokens past the chunk end
@@ -192,10 +244,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int tk = n * 8 + 2 * (lane & 3) + (c & 1);
-                        s[n][c] = tk < valid ? s[n][c] * p.scale_log2 : -INFINITY;
+                        sc[n][c] = tk < valid ? sc[n][c] * p.scale_log2 : -INFINITY;
                     }
-                    mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-                    mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+                    mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
                 }
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -210,19 +262,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
                 float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
                 for (int n = 0; n < 2; ++n) {
-                    ps[n][0] = exp2f(s[n][0] - ref0);
-                    ps[n][1] = exp2f(s[n][1] - ref0);
-                    ps[n][2] = exp2f(s[n][2] - ref1);
-                    ps[n][3] = exp2f(s[n][3] - ref1);
+                    ps[n][0] = exp2f(sc[n][0] - ref0);
+                    ps[n][1] = exp2f(sc[n][1] - ref0);
+                    ps[n][2] = exp2f(sc[n][2] - ref1);
+                    ps[n][3] = exp2f(sc[n][3] - ref1);
                     sum0 += ps[n][0] + ps[n][1];
                     sum1 += ps[n][2] + ps[n][3];
                 }
                 l0 = l0 * a0 + sum0;
                 l1 = l1 * a1 + sum1;
+                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-                for (int n = 0; n < D / 8; ++n) {
-                    acc[n][0] *= a0; acc[n][1] *= a0;
-                    acc[n][2] *= a1; acc[n][3] *= a1;
+                    for (int n = 0; n < D / 8; ++n) {
+                        acc[n][0] *= a0; acc[n][1] *= a0;
+                        acc[n][2] *= a1; acc[n][3] *= a1;
+                    }
                 }
                 uint32_t pa[4];
                 pa[0] = pack_bf16(ps[0][0], ps[0][1]);
@@ -231,17 +285,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
                 pa[3] = pack_bf16(ps[1][2], ps[1][3]);
                 {
                     const int mi = lane >> 3;
-                    const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
+                    const uint32_t rowaddr = vb + (uint32_t)(warp * 16 + (mi & 1) * 8 + (lane & 7)) * LY::kPitch +
+                                             (uint32_t)(mi >> 1) * 16;
 #pragma unroll
                     for (int nd = 0; nd < D / 16; ++nd) {
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vb + swz<D>(row, nd * 2 + (mi >> 1)), b0, b1, b2, b3);
+                        ldmatrix_x4_trans(rowaddr + nd * 32, b0, b1, b2, b3);
                         mma_bf16_16816(acc[2 * nd], pa, b0, b1);
                         mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
                     }
                 }
             }
-            __syncthreads();
+            __syncwarp();
+            if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
         }
 
         // ---- merge the four warps' states; write the output or a partial ----
@@ -249,7 +305,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        float *scratch = reinterpret_cast<float *>(smem + ((j + kStages - 1) % kStages) * LY::kStageBytes);
         if ((lane & 3) == 0) {
             stats[(warp * 16 + r0) * 2 + 0] = m0;
             stats[(warp * 16 + r0) * 2 + 1] = l0;
@@ -262,17 +317,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
             *reinterpret_cast<float2 *>(scratch + (warp * 16 + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
             *reinterpret_cast<float2 *>(scratch + (warp * 16 + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
         }
-        __syncthreads();
-        for (int e = tid; e < g * D; e += kDecThreads) {
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(merge_in);
+        if (!__all_sync(0xffffffffu, wait_or_abort(merge_in, merges & 1, abort_flag, status, kStatusMergeWait))) return;
+        for (int e = warp * 32 + lane; e < g * D; e += kConsumers * 32) {
             const int row = e / D, d = e - row * D;
             float M = -INFINITY;
 #pragma unroll
-            for (int ww = 0; ww < kDecWarps; ++ww) M = fmaxf(M, stats[(ww * 16 + row) * 2]);
+            for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, stats[(ww * 16 + row) * 2]);
             float val = 0.f, lse_v = -INFINITY;
             if (M != -INFINITY) {
                 float L = 0.f, num = 0.f;
 #pragma unroll
-                for (int ww = 0; ww < kDecWarps; ++ww) {
+                for (int ww = 0; ww < kConsumers; ++ww) {
                     const float f = exp2f(stats[(ww * 16 + row) * 2] - M);
                     L += stats[(ww * 16 + row) * 2 + 1] * f;
                     num += scratch[(ww * 16 + row) * D + d] * f;
@@ -290,9 +347,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_bf16_kernel(const Decod
                 if (d == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
             }
         }
-        __syncthreads();
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(merge_out);
+        if (!__all_sync(0xffffffffu, wait_or_abort(merge_out, merges & 1, abort_flag, status, kStatusMergeWait))) return;
+        ++merges;
     }
-    cp_async_wait<0>();
 }
 
 // fp32 decode: CUDA-core fp32 arithmetic, one warp per fused row, lanes over
@@ -421,7 +480,7 @@ int launch_decode_bf16(const DecodeParams &p, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
         configured[dev] = true;
     }
-    decode_bf16_kernel<D><<<grid, kDecThreads, DecodeLayout<D>::kSmemBytes, stream>>>(p);
+    decode_bf16_kernel<D><<<grid, kWsThreads, DecodeLayout<D>::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
     return BSP_OK;
@@ -449,7 +508,7 @@ int launch_reduce_t(const ReduceParams &p, cudaStream_t stream) {
 
 int decode_ctas_per_sm(int head_dim, int dtype) {
     if (dtype != BSP_DTYPE_BF16) return 4;
-    return 2;  // 3 x 32 KB (D = 128) or 3 x 16 KB ring per CTA; 2 CTAs keep ~190 KB of copies in flight per SM
+    return 1;  // a 5-stage ring of 64-token K+V stages (~174 KB at D = 128) per SM
 }
 
 int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
@@ -462,6 +521,7 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     p.off_items = plan->off_items;
     p.off_plse = plan->off_partial_lse;
     p.off_po = plan->off_partial_o;
+    p.off_status = plan->off_status;
     p.q = q; p.k = k_pages; p.v = v_pages;
     p.kv_indices = kv_indices;
     p.o = o;
