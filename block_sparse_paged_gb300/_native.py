@@ -55,7 +55,7 @@ class PlanInfo(ctypes.Structure):
                 ("off_items", ctypes.c_uint64), ("off_merges", ctypes.c_uint64), ("off_status", ctypes.c_uint64),
                 ("off_partial_lse", ctypes.c_uint64), ("off_partial_o", ctypes.c_uint64),
                 ("metadata_bytes", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64),
-                ("valid", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("valid", ctypes.c_int32), ("num_qo_tokens", ctypes.c_int32)]
 
 
 # numpy views of the plan's staging image (bsp_work_item, bsp_merge_entry)

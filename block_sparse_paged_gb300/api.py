@@ -163,7 +163,8 @@ class PagedAttention:
             lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
         dev = self.device
         args = [ctypes.byref(self.info), _dev(q, "q", self.dtype, dev), _dev(k_pages, "k_pages", self.dtype, dev),
-                _dev(v_pages, "v_pages", self.dtype, dev), _dev(kv_indices, "kv_indices", torch.int32, dev)]
+                _dev(v_pages, "v_pages", self.dtype, dev), _dev(kv_indices, "kv_indices", torch.int32, dev)
+                if kv_indices.numel() else None]
         tail = [ctypes.c_float(sm_scale), _dev(out, "out", self.dtype, dev),
                 None if lse is None else _dev(lse, "lse", torch.float32, dev),
                 ctypes.c_void_p(self.workspace.data_ptr())]

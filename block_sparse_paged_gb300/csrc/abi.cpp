@@ -67,7 +67,7 @@ extern "C" int bsp_decode_run(const bsp_plan_info *plan, const void *q, const vo
     clear_error();
     int rc = check_plan(plan, BSP_MODE_DECODE, workspace);
     if (rc != BSP_OK) return rc;
-    if (!q || !k_pages || !v_pages || !kv_indices || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, workspace, stream);
     if (rc != BSP_OK) return rc;
     return launch_reduce(plan, o, lse, workspace, stream);
@@ -79,7 +79,7 @@ extern "C" int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const v
     clear_error();
     int rc = check_plan(plan, BSP_MODE_PREFILL, workspace);
     if (rc != BSP_OK) return rc;
-    if (!q || !k_pages || !v_pages || !kv_indices || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (num_pages < 1) return fail(BSP_ERR_INVALID_ARG, "num_pages must be positive");
     rc = launch_prefill(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
     if (rc != BSP_OK) return rc;
@@ -94,7 +94,7 @@ extern "C" int bsp_run_attention(const bsp_plan_info *plan, const void *q, const
     const int mode = plan->problem.mode;
     int rc = check_plan(plan, mode, workspace);
     if (rc != BSP_OK) return rc;
-    if (!q || !k_pages || !v_pages || !kv_indices || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (mode == BSP_MODE_DECODE)
         return launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, workspace, stream);
     if (num_pages < 1) return fail(BSP_ERR_INVALID_ARG, "num_pages must be positive");

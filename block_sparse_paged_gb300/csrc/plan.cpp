@@ -294,6 +294,7 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
     o.off_partial_o = lay.off_partial_o;
     o.metadata_bytes = lay.metadata_end;
     o.workspace_bytes = lay.total;
+    o.num_qo_tokens = qo[batch];
     o.valid = ws ? 1 : 2;  // 2: host-only plan, not runnable
     return BSP_OK;
 }

@@ -1,12 +1,491 @@
-// Ragged causal prefill on the tensor cores (placeholder until the tcgen05
-// kernel lands).
+// Ragged (causal) prefill over a paged KV cache on the tcgen05 tensor cores.
+//
+// What it computes (FlashInfer: Making Attention Fit the Serving Workload,
+// §2.1 eq 1, §3.1 eq 4-5): for each work item of the plan — a query tile of
+// 128 packed rows (positions x the g query heads of one kv head, technical
+// review eq 3) and one chunk of that tile's visible KV — the attention state
+// (O, LSE) over the chunk, with the bottom-right causal mask (FlashInfer 原理
+// overview, ⑧). Unsplit tiles write the final output, split ones an fp32
+// partial state that the reduction kernel merges (overview ⑨).
+//
+// How (sparse gather, dense compute: overview ⑥, engineering walkthrough
+// §IV.2 and §V.4): the KV chunk is walked in tiles of 128 tokens. Rows are
+// contiguous inside a page, so each page (or 128-token piece of a page) of K
+// and V is one TMA tensor copy into a 128-byte-swizzled shared-memory tile;
+// the page table only supplies the copy's row coordinate. One CTA per SM,
+// persistent over its plan queue, six warps:
+//   warp 0     TMA: the Q tile of the item, then K/V tiles into a 2-stage ring
+//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M 128, N 128, K 128) into
+//              TMEM, then O += P V (P from shared memory, V as an MN-major
+//              operand) into TMEM
+//   warps 2-5  one thread per row: scale, mask, online softmax in base 2,
+//              P (bf16) to shared memory, rescale of O in TMEM when the row
+//              maximum moves, and the epilogue O / l, LSE.
+// S is read out of TMEM before the next S is issued, so the next QK^T runs
+// while the softmax of this tile finishes; PV of this tile runs while the
+// softmax of the next one computes its exponentials.
+// Every wait is bounded (counted polls with a suspend hint); a wait that gives
+// up sets the workspace status word and an abort flag, and the CTA finishes
+// without further work.
+#include <cuda.h>
+
+#include <climits>
+#include <cstring>
+#include <mutex>
+
 #include "bsp_internal.h"
+#include "device_common.cuh"
+#include "sm100.cuh"
 
 namespace bsp {
+namespace {
 
-int launch_prefill(const bsp_plan_info *, const void *, const void *, const void *, const int32_t *, int64_t,
-                   float, void *, float *, void *, cudaStream_t) {
-    return fail(BSP_ERR_UNSUPPORTED, "prefill kernel not built yet");
+using namespace sm100;
+
+constexpr int kRows = 128;        // packed query rows per tile
+constexpr int kKvTile = 128;      // KV tokens per tile
+constexpr int kD = 128;           // head dim
+constexpr int kKvStages = 2;
+constexpr int kThreads = 192;
+constexpr int kHalf = 16384;      // [128 rows][64 bf16], 128-byte swizzle
+constexpr int kTile = 2 * kHalf;  // [128 rows][128 bf16]
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kKvStages * kTile;
+constexpr int kOffP = kOffV + kKvStages * kTile;
+constexpr int kOffBar = kOffP + kTile;
+enum Bar { kQFull = 0, kQEmpty, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull, kSFree, kPFull, kODone, kOFree, kNumBars };
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
+static_assert(kSmemBytes <= 227 * 1024, "prefill tiles exceed shared memory");
+
+constexpr uint32_t kTmemCols = 256;  // S at [0, 128), O at [128, 256)
+constexpr uint32_t kWaitHintNs = 100000;
+constexpr uint32_t kWaitPolls = 10000;  // about 1 s
+constexpr int kStatusWait = 0x201;
+
+struct PrefillParams {
+    const uint8_t *ws;
+    uint64_t off_queue, off_items, off_plse, off_po, off_status;
+    const int32_t *kv_indices;
+    void *o;
+    float *lse;
+    float scale_log2;
+    int H_qo, g, page_size, box_rows, causal, tile_rows;
+};
+
+struct Ctx {
+    volatile int *abort_flag;
+    int *status;
+};
+
+__device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
+        if (*c.abort_flag) return false;
+    }
+    *c.abort_flag = 1;
+    atomicCAS(c.status, 0, kStatusWait);
+    return false;
+}
+// Same, with one outcome for the whole warp.
+__device__ __forceinline__ bool wait_bar_warp(const Ctx &c, uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_bar(c, bar, parity));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = dev::smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
+    const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
+    const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
+    if (it0 >= it1) return;  // uniform across the CTA, before any barrier
+
+    auto bar = [&](int i) { return sb + kOffBar + 8u * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
+    Ctx ctx{reinterpret_cast<volatile int *>(smem + kOffAbort),
+            reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + p.off_status)};
+
+    if (tid == 0) {
+        mbar_init(bar(kQFull), 1);
+        mbar_init(bar(kQEmpty), 1);
+        mbar_init(bar(kKvFull0), 1);
+        mbar_init(bar(kKvFull1), 1);
+        mbar_init(bar(kKvEmpty0), 1);
+        mbar_init(bar(kKvEmpty1), 1);
+        mbar_init(bar(kSFull), 1);
+        mbar_init(bar(kSFree), 128);
+        mbar_init(bar(kPFull), 128);
+        mbar_init(bar(kODone), 1);
+        mbar_init(bar(kOFree), 128);
+        *ctx.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(dev::smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int g = p.g;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        int q_cnt = 0, kv_cnt = 0;
+        for (int it = it0; it < it1 && !*ctx.abort_flag; ++it) {
+            const bsp_work_item w = items[it];
+            const int len = w.kv_end - w.kv_start;
+            const int nt = (len + kKvTile - 1) / kKvTile;
+            if (nt == 0) continue;
+            if (!wait_bar_warp(ctx, bar(kQEmpty), (q_cnt & 1) ^ 1)) break;
+            ++q_cnt;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(kQFull), kTile);
+                tma_load_3d(sb + kOffQ, &tq, bar(kQFull), 0, w.kv_head * g, w.q_tok0);
+                tma_load_3d(sb + kOffQ + kHalf, &tq, bar(kQFull), 64, w.kv_head * g, w.q_tok0);
+            }
+            bool ok = true;
+            for (int t = 0; t < nt && ok; ++t, ++kv_cnt) {
+                const int tok0 = w.kv_start + t * kKvTile;
+                const int valid = min(kKvTile, len - t * kKvTile);
+                const int nseg = (valid + p.box_rows - 1) / p.box_rows;
+                int page = 0;
+                if (lane < nseg) page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
+                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
+                ok = wait_bar_warp(ctx, bar(kKvEmpty0 + stage), (round & 1) ^ 1);
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kKvFull0 + stage), (uint32_t)nseg * p.box_rows * 128 * 4);
+                __syncwarp();
+                if (lane < nseg) {
+                    const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
+                    const uint32_t off = (uint32_t)lane * p.box_rows * 128;
+                    const uint32_t dk = sb + kOffK + stage * kTile + off, dv = sb + kOffV + stage * kTile + off;
+                    tma_load_3d(dk, &tk, bar(kKvFull0 + stage), 0, w.kv_head, row0);
+                    tma_load_3d(dk + kHalf, &tk, bar(kKvFull0 + stage), 64, w.kv_head, row0);
+                    tma_load_3d(dv, &tv, bar(kKvFull0 + stage), 0, w.kv_head, row0);
+                    tma_load_3d(dv + kHalf, &tv, bar(kKvFull0 + stage), 64, w.kv_head, row0);
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        constexpr uint32_t id_s = idesc_bf16_f32(kRows, kKvTile, false, false);
+        constexpr uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
+        const uint32_t tS = tmem, tO = tmem + 128;
+        int q_cnt = 0, kv_cnt = 0, s_cnt = 0, p_cnt = 0, done = 0;
+        bool ok = true;
+        for (int it = it0; it < it1 && ok; ++it) {
+            const bsp_work_item w = items[it];
+            const int nt = (w.kv_end - w.kv_start + kKvTile - 1) / kKvTile;
+            if (nt == 0) continue;
+            if (!(ok = wait_bar_warp(ctx, bar(kQFull), q_cnt & 1))) break;
+            ++q_cnt;
+            for (int t = 0; t < nt; ++t, ++kv_cnt) {
+                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
+                if (!(ok = wait_bar_warp(ctx, bar(kKvFull0 + stage), round & 1))) break;
+                if (!(ok = wait_bar_warp(ctx, bar(kSFree), (s_cnt & 1) ^ 1))) break;
+                ++s_cnt;
+                tc_fence_after();
+                const uint32_t sK = sb + kOffK + stage * kTile, sV = sb + kOffV + stage * kTile;
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        mma_bf16_ss(tS, smem_desc_sw128(sb + kOffQ + o, 16, 1024), smem_desc_sw128(sK + o, 16, 1024),
+                                    id_s, kk > 0);
+                    }
+                    mma_commit(bar(kSFull));
+                    if (t == nt - 1) mma_commit(bar(kQEmpty));
+                }
+                __syncwarp();
+                if (!(ok = wait_bar_warp(ctx, bar(kPFull), p_cnt & 1))) break;
+                ++p_cnt;
+                if (t == 0 && done > 0 && !(ok = wait_bar_warp(ctx, bar(kOFree), (done - 1) & 1))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                        const uint32_t po = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        mma_bf16_ss(tO, smem_desc_sw128(sb + kOffP + po, 16, 1024),
+                                    smem_desc_sw128(sV + kk * 16 * 128, kHalf, 1024), id_pv, (t > 0 || kk > 0));
+                    }
+                    mma_commit(bar(kODone));
+                    mma_commit(bar(kKvEmpty0 + stage));
+                }
+                __syncwarp();
+            }
+            ++done;
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const uint32_t tl = (uint32_t)(q4 * 32) << 16;
+        const uint32_t tS = tmem + tl, tO = tmem + tl + 128;
+        float *plse = reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse);
+        float *po = reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_po);
+        int s_cnt = 0, pv_cnt = 0, kv_cnt = 0;
+        bool ok = true;
+        for (int it = it0; it < it1 && ok; ++it) {
+            const bsp_work_item w = items[it];
+            const int len = w.kv_end - w.kv_start;
+            const int nt = (len + kKvTile - 1) / kKvTile;
+            const int pos = w.pos0 + r / g;
+            const int lim = p.causal ? pos + w.kv_len - w.qo_len : INT_MAX;  // key j allowed iff j <= lim
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < nt; ++t, ++kv_cnt) {
+                const int tok0 = w.kv_start + t * kKvTile;
+                const int valid = min(kKvTile, len - t * kKvTile);
+                if (!(ok = wait_bar_warp(ctx, bar(kSFull), s_cnt & 1))) break;
+                ++s_cnt;
+                tc_fence_after();
+                float sv[kKvTile];
+#pragma unroll
+                for (int c = 0; c < kKvTile / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tS + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(kSFree));
+                // scale, mask, running max
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKvTile; ++c) {
+                    const bool allowed = c < valid && tok0 + c <= lim;
+                    sv[c] = allowed ? sv[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[c]);
+                }
+                const float mn = fmaxf(m, mx);
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                const float alpha = exp2f(m - ref);
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < kKvTile; ++c) {
+                    sv[c] = exp2f(sv[c] - ref);
+                    sum += sv[c];
+                }
+                l = l * alpha + sum;
+                m = mn;
+                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
+                if (valid < kKvTile) {
+                    // rows past the chunk end: zero V so that P = 0 meets finite values
+                    if (!(ok = wait_bar_warp(ctx, bar(kKvFull0 + stage), round & 1))) break;
+                    if (r >= valid) {
+                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + stage * kTile + r * 128);
+                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + stage * kTile + kHalf + r * 128);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // the previous PV must be done before P is overwritten and O rescaled
+                if (t > 0) {
+                    if (!(ok = wait_bar_warp(ctx, bar(kODone), pv_cnt & 1))) break;
+                    ++pv_cnt;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int ch = 0; ch < kKvTile / 8; ++ch) {
+                    uint4 u;
+                    u.x = dev::pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
+                    u.y = dev::pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
+                    u.z = dev::pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
+                    u.w = dev::pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
+                    const int half = ch >> 3, kc = ch & 7;
+                    *reinterpret_cast<uint4 *>(smem + kOffP + half * kHalf + r * 128 + ((kc ^ (r & 7)) << 4)) = u;
+                }
+                if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        float v[32];
+                        tmem_ld32(tO + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tmem_st32(tO + c * 32, v);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(kPFull));
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l, LSE; final output or partial state ----
+            if (nt > 0) {
+                if (!(ok = wait_bar_warp(ctx, bar(kODone), pv_cnt & 1))) break;
+                ++pv_cnt;
+                tc_fence_after();
+            }
+            const bool row_ok = r < w.n_pos * g;
+            const bool has = l > 0.f;
+            const float inv = has ? 1.f / l : 0.f;
+            const float lse_v = has ? (m + log2f(l)) * dev::kLn2 : -INFINITY;
+            const size_t orow = (size_t)(w.q_tok0 + r / g) * p.H_qo + (size_t)w.kv_head * g + (r % g);
+            const size_t prow = (size_t)w.slot * p.tile_rows + r;
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                float v[32];
+                if (nt > 0) {
+                    tmem_ld32(tO + c * 32, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                if (row_ok) {
+                    if (w.slot < 0) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + orow * kD + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 u;
+                            u.x = dev::pack_bf16(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
+                            u.y = dev::pack_bf16(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
+                            u.z = dev::pack_bf16(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
+                            u.w = dev::pack_bf16(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
+                            dst[q] = u;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(po + prow * kD + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(v[q * 4] * inv, v[q * 4 + 1] * inv, v[q * 4 + 2] * inv, v[q * 4 + 3] * inv);
+                    }
+                }
+            }
+            if (row_ok) {
+                if (w.slot < 0) {
+                    if (p.lse) p.lse[orow] = lse_v;
+                } else {
+                    plse[prow] = lse_v;
+                }
+            }
+            if (nt > 0) {
+                tc_fence_before();
+                mbar_arrive(bar(kOFree));
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (*ctx.abort_flag) {
+        // let copies and MMAs already in flight finish before TMEM is released
+        for (int i = 0; i < 100; ++i) __nanosleep(1000);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host: tensor maps -----------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 3-D bf16 map (D innermost, then heads, then rows), 64-element x b1 x b2 box, 128-byte swizzle.
+int make_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows, uint32_t box_heads,
+             uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(BSP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return fail(BSP_ERR_INVALID_ARG, "tensor base not 16-byte aligned");
+    cuuint64_t dims[3] = {(cuuint64_t)kD, heads, rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, heads * kD * 2};
+    cuuint32_t box[3] = {64, box_heads, box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    std::memset(map, 0, sizeof(*map));
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(BSP_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return BSP_OK;
+}
+
+}  // namespace
+
+int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                   const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
+                   void *workspace, cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    const int g = plan->group;
+    if (P.dtype != BSP_DTYPE_BF16) return fail(BSP_ERR_UNSUPPORTED, "prefill supports bf16 only");
+    if (P.head_dim != kD) return fail(BSP_ERR_UNSUPPORTED, "prefill supports head_dim 128 only");
+    if (P.page_size < 8 || (P.page_size & (P.page_size - 1)) != 0)
+        return fail(BSP_ERR_UNSUPPORTED, "prefill needs page_size a power of two >= 8");
+    if (plan->tile_rows != kRows || kRows % g != 0) return fail(BSP_ERR_UNSUPPORTED, "prefill needs 128 % g == 0");
+    if (num_pages * (int64_t)P.page_size > INT32_MAX) return fail(BSP_ERR_UNSUPPORTED, "KV pool beyond 2^31 rows");
+
+    CUtensorMap tq, tk, tv;
+    const int box_rows = P.page_size < kKvTile ? P.page_size : kKvTile;
+    int rc = make_map(&tq, q, P.num_qo_heads, (uint64_t)(plan->num_qo_tokens > 0 ? plan->num_qo_tokens : 1), g,
+                      kRows / g);
+    if (rc == BSP_OK) rc = make_map(&tk, k_pages, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
+    if (rc == BSP_OK) rc = make_map(&tv, v_pages, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
+    if (rc != BSP_OK) return rc;
+
+    PrefillParams p;
+    p.ws = static_cast<const uint8_t *>(workspace);
+    p.off_queue = plan->off_queue_indptr;
+    p.off_items = plan->off_items;
+    p.off_plse = plan->off_partial_lse;
+    p.off_po = plan->off_partial_o;
+    p.off_status = plan->off_status;
+    p.kv_indices = kv_indices;
+    p.o = o;
+    p.lse = lse;
+    p.scale_log2 = sm_scale * dev::kLog2e;
+    p.H_qo = P.num_qo_heads;
+    p.g = g;
+    p.page_size = P.page_size;
+    p.box_rows = box_rows;
+    p.causal = P.causal;
+    p.tile_rows = plan->tile_rows;
+
+    static bool configured[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill smem attribute: ") + cudaGetErrorString(e));
+        configured[dev] = true;
+    }
+    prefill_kernel<<<plan->capacity.num_ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
 }
 
 }  // namespace bsp

@@ -150,7 +150,7 @@ typedef struct bsp_plan_info {
     uint64_t metadata_bytes; /* bytes copied host -> device per plan          */
     uint64_t workspace_bytes;
     int32_t valid;           /* 1: planned and copied; 2: host-only plan      */
-    int32_t reserved;
+    int32_t num_qo_tokens;   /* qo_indptr[batch]: rows of q and o             */
 } bsp_plan_info;
 
 /* Number of persistent CTAs the attention kernel of `mode` wants on `device`
@@ -210,7 +210,7 @@ int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity, int32_t b
  *   k_pages,
  *   v_pages     device, [num_pages, page_size, H_kv, D]
  *   kv_indices  device, int32, the page ids (same array the plan's indptr
- *               indexes)
+ *               indexes); may be NULL when no request has a page
  *   sm_scale    score scale (usually 1/sqrt(D))
  *   o           device, [n_tokens, H_qo, D], written
  *   lse         device, float [n_tokens, H_qo], written; may be NULL

@@ -1,0 +1,93 @@
+"""Prefill path (tcgen05) and the composable shared-prefix path on the GPU,
+through the C ABI, against the oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import compare, lib, oracle_full, run_batch, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    return lib()
+
+
+CASES = [
+    # (seed, qo lens, kv lens, H_qo, H_kv, page, causal, num_ctas)
+    (1, [1, 17, 128, 129, 300], [1, 17, 128, 129, 300], 32, 8, 16, True, 152),
+    (2, [200, 64, 1000], [200, 64, 1000], 32, 8, 16, True, 7),           # splits + merges
+    (3, [33, 5, 260], [100, 5, 900], 8, 8, 8, True, 13),                 # qo < kv (prefix cached)
+    (4, [70, 300], [20, 128], 16, 2, 32, True, 5),                       # qo > kv: rows with no key
+    (5, [64, 190, 3], [500, 190, 77], 16, 16, 128, False, 9),            # non-causal, g = 1
+    (6, [128, 257], [128, 257], 64, 8, 16, True, 3),                     # g = 8
+    (7, [1], [0], 32, 8, 16, True, 4),                                   # empty KV
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
+def test_random_prefill(bsp, case):
+    seed, qo, kv, hq, hk, ps, causal, C = case
+    b = workloads.paged_batch(seed, qo, kv, hq, hk, 128, ps, "bf16", causal=causal, extra_pages=2)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=C)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_ragged_causal_prefill_full_size(bsp):
+    """16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, causal;
+    sampled rows against the oracle; two runs bitwise equal."""
+    b = workloads.ragged_causal_prefill_bf16()
+    out, lse, pa = run_batch(bsp, b, mode="prefill")
+    tok, head = sample_rows(b, 384, 21)
+    O, L = oracle.attention_rows_of(b, tok, head)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    q, k, v, idx = to_dev(b)
+    out2, lse2 = pa.run(q, k, v, idx, b.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert pa.check_device_error() == 0
+
+
+def composable_decode(bsp, sp, num_ctas_prefill=None, num_ctas_decode=None):
+    """Prefix view (all queries as one row block over the shared pages, on the
+    prefill kernel) and suffix view (decode), merged with merge_state."""
+    dev = "cuda"
+    q = sp.full.q.to(dev)
+    k = sp.full.k_pages.to(dev)
+    v = sp.full.v_pages.to(dev)
+    pre = bsp.PagedAttention("prefill", 32, 8, 128, sp.full.page_size, False, torch.bfloat16, max_batch=1,
+                             max_qo_tokens=sp.prefix.batch * 0 + int(sp.prefix.qo_indptr[-1]),
+                             num_ctas=num_ctas_prefill)
+    pre.plan(sp.prefix.kv_indptr, sp.prefix.last_page_len, qo_indptr=sp.prefix.qo_indptr)
+    suf = bsp.PagedAttention("decode", 32, 8, 128, sp.full.page_size, False, torch.bfloat16,
+                             max_batch=sp.suffix.batch, num_ctas=num_ctas_decode)
+    suf.plan(sp.suffix.kv_indptr, sp.suffix.last_page_len)
+    o1, l1 = pre.run(q, k, v, torch.from_numpy(sp.prefix.kv_indices).to(dev), sp.full.sm_scale)
+    o2, l2 = suf.run(q, k, v, torch.from_numpy(sp.suffix.kv_indices).to(dev), sp.full.sm_scale)
+    out, lse = bsp.merge_state(o1, l1, o2, l2)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def test_shared_prefix_composable_small(bsp):
+    sp = workloads.shared_prefix_decode_bf16(batch=6, prefix_len=512, outlier=700, suffix_lo=1, suffix_hi=90,
+                                             seed=51)
+    out, lse = composable_decode(bsp, sp, num_ctas_prefill=5, num_ctas_decode=7)
+    O, L = oracle_full(sp.full)
+    compare(out, lse, O, L, "bf16")
+
+
+def test_shared_prefix_composable_full_size(bsp):
+    """64 requests sharing an 8192-token prefix, suffixes U{64..1024} and one
+    32768 outlier: prefix view + suffix view + merge equals attention over the
+    full page lists (sampled rows)."""
+    sp = workloads.shared_prefix_decode_bf16()
+    out, lse = composable_decode(bsp, sp)
+    tok, head = sample_rows(sp.full, 256, 22)
+    O, L = oracle.attention_rows_of(sp.full, tok, head)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))
