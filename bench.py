@@ -424,7 +424,71 @@ def secondary(bsp, dev, args, pk):
                                         "flops": fl, "attn_ms": round(attn, 4), "merge_ms": round(merge, 4)}
     except Exception as e:  # the prefill kernel may not be built for this shape
         res["ragged_causal_prefill"] = {"unavailable": str(e)[:200]}
+    del b
+    torch.cuda.empty_cache()
+    res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
     return res
+
+
+def shared_prefix_bytes(sp) -> int:
+    """Prefix KV once, every suffix's KV, Q, O, LSE and both page tables."""
+    e = 2
+    kvrow = sp.full.num_kv_heads * sp.full.head_dim * e * 2
+    n_tok = int(sp.full.qo_indptr[-1])
+    qo = 2 * n_tok * sp.full.num_qo_heads * sp.full.head_dim * e
+    lse = n_tok * sp.full.num_qo_heads * 4
+    meta = 4 * (len(sp.prefix.kv_indices) + len(sp.suffix.kv_indices) + 3 * (sp.full.batch + 1))
+    return sp.prefix_len * kvrow + int(sp.suffix_lens.sum()) * kvrow + qo + lse + meta
+
+
+def shared_prefix(bsp, dev, steps, warm, pk):
+    """Composable decode: prefix view on the prefill kernel (all 64 queries as one
+    row block over the shared pages), suffix view on the decode kernel, then
+    merge_state; timed as the three launches plus both merges of partials."""
+    import workloads
+    sp = workloads.shared_prefix_decode_bf16()
+    q = sp.full.q.to(dev)
+    k = sp.full.k_pages.to(dev)
+    v = sp.full.v_pages.to(dev)
+    ip = torch.from_numpy(sp.prefix.kv_indices).to(dev)
+    isf = torch.from_numpy(sp.suffix.kv_indices).to(dev)
+    pre = bsp.PagedAttention("prefill", 32, 8, 128, sp.full.page_size, False, torch.bfloat16, max_batch=1,
+                             max_qo_tokens=int(sp.prefix.qo_indptr[-1]), device=dev)
+    suf = bsp.PagedAttention("decode", 32, 8, 128, sp.full.page_size, False, torch.bfloat16,
+                             max_batch=sp.suffix.batch, device=dev)
+    pre.plan(sp.prefix.kv_indptr, sp.prefix.last_page_len, qo_indptr=sp.prefix.qo_indptr)
+    suf.plan(sp.suffix.kv_indptr, sp.suffix.last_page_len)
+    o1 = torch.empty_like(q)
+    o2 = torch.empty_like(q)
+    l1 = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    l2 = torch.empty_like(l1)
+    out = torch.empty_like(q)
+    lse = torch.empty_like(l1)
+
+    def run():
+        pre.run(q, k, v, ip, sp.full.sm_scale, out=o1, lse=l1)
+        suf.run(q, k, v, isf, sp.full.sm_scale, out=o2, lse=l2)
+        bsp.merge_state(o1, l1, o2, l2, out=out, lse_out=lse)
+
+    for _ in range(warm):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = shared_prefix_bytes(sp)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    n, P, S = sp.full.batch, sp.prefix_len, float(sp.suffix_lens.mean())
+    ratio = n * (P + S) / (P + n * S)
+    return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
+            "algorithmic_bytes": nbytes, "launches_per_step": 5,
+            "eq15_traffic_ratio": round(ratio, 3),
+            "workload": "64 decode requests sharing an 8192-token prefix, suffixes U{64..1024} and one 32768 "
+                        "outlier, page 16, 32/8 heads, D 128, bf16"}
 
 
 # ---------------------------------------------------------------------------

@@ -12,7 +12,7 @@
 
 namespace bsp {
 
-constexpr int kPrefillTileRows = 128;   // packed query rows per prefill tile
+constexpr int kPrefillTileRows = 256;   // packed query rows per prefill tile (two 128-row MMA subtiles)
 constexpr int kMaxDecodeGroup = 16;     // decode tile: M = 16 rows of the MMA
 constexpr uint64_t kAlign = 256;
 

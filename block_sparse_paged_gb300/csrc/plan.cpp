@@ -30,7 +30,7 @@ bool check_problem(const bsp_problem *p) {
     if (p->dtype != BSP_DTYPE_BF16 && p->dtype != BSP_DTYPE_F32)
         return fail(BSP_ERR_INVALID_ARG, "dtype must be BSP_DTYPE_BF16 or BSP_DTYPE_F32"), false;
     const int g = p->num_qo_heads / p->num_kv_heads;
-    if (p->mode == BSP_MODE_PREFILL && kPrefillTileRows % g != 0)
+    if (p->mode == BSP_MODE_PREFILL && (kPrefillTileRows / 2) % g != 0)
         return fail(BSP_ERR_UNSUPPORTED, "prefill needs 128 % (num_qo_heads / num_kv_heads) == 0"), false;
     return true;
 }
@@ -44,7 +44,7 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
     l.group = g;
     l.tile_rows = p->mode == BSP_MODE_DECODE ? g : kPrefillTileRows;
     // Query tiles per kv head: decode tiles are one position each; prefill
-    // tiles hold 128 / g positions, so sum_b ceil(qo_b g / 128) <= tokens g / 128 + B.
+    // tiles hold 256 / g positions, so sum_b ceil(qo_b g / 256) <= tokens g / 256 + B.
     const int64_t tiles_per_head = p->mode == BSP_MODE_DECODE
         ? c->max_qo_tokens
         : (c->max_qo_tokens * g + kPrefillTileRows - 1) / kPrefillTileRows + c->max_batch;

@@ -2,7 +2,7 @@
 //
 // What it computes (FlashInfer: Making Attention Fit the Serving Workload,
 // §2.1 eq 1, §3.1 eq 4-5): for each work item of the plan — a query tile of
-// 128 packed rows (positions x the g query heads of one kv head, technical
+// 256 packed rows (positions x the g query heads of one kv head, technical
 // review eq 3) and one chunk of that tile's visible KV — the attention state
 // (O, LSE) over the chunk, with the bottom-right causal mask (FlashInfer 原理
 // overview, ⑧). Unsplit tiles write the final output, split ones an fp32
@@ -11,19 +11,28 @@
 // How (sparse gather, dense compute: overview ⑥, engineering walkthrough
 // §IV.2 and §V.4): the KV chunk is walked in tiles of 128 tokens. Rows are
 // contiguous inside a page, so each page (or 128-token piece of a page) of K
-// and V is one TMA tensor copy into a 128-byte-swizzled shared-memory tile;
-// the page table only supplies the copy's row coordinate. One CTA per SM,
-// persistent over its plan queue, six warps:
-//   warp 0     TMA: the Q tile of the item, then K/V tiles into a 2-stage ring
-//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M 128, N 128, K 128) into
-//              TMEM, then O += P V (P from shared memory, V as an MN-major
-//              operand) into TMEM
-//   warps 2-5  one thread per row: scale, mask, online softmax in base 2,
-//              P (bf16) to shared memory, rescale of O in TMEM when the row
-//              maximum moves, and the epilogue O / l, LSE.
-// S is read out of TMEM before the next S is issued, so the next QK^T runs
-// while the softmax of this tile finishes; PV of this tile runs while the
-// softmax of the next one computes its exponentials.
+// and of V is one TMA tensor copy into a 128-byte-swizzled shared-memory tile;
+// the page table only supplies the copy's row coordinate. The 256 query rows
+// are two 128-row MMA subtiles that share every K and V tile. One CTA per SM,
+// persistent over its plan queue, ten warps:
+//   warp 0      TMA: both Q subtiles of the item, then K and V tiles into two
+//               separate 2-stage rings (K is released after the second S, V
+//               after the second PV)
+//   warp 1      TMEM owner and MMA issuer, in the order
+//               S0(0) S1(0) | PV0(t) S0(t+1) PV1(t) S1(t+1) | ...
+//               S = Q K^T (M 128, N 128, K 128) into TMEM; P (bf16) is written
+//               back over S in TMEM and O += P V takes P straight from TMEM
+//               (V as an MN-major shared-memory operand)
+//   warps 2-5   softmax of subtile 0, warps 6-9 softmax of subtile 1: one thread
+//               per row; scale, mask (only on tiles that need it), base-2 online
+//               softmax, P to TMEM, O rescale in TMEM, epilogue O / l and LSE.
+// While one softmax group works on its S, the tensor core runs the other
+// subtile's PV and next S. The reference maximum of a row is only moved when
+// the running maximum exceeds it by more than 8 (a factor 256): the result is
+// exact because O and l always share the same reference, and O in TMEM is
+// rescaled only then. MMAs of the CTA execute in issue order, so S(t+1) cannot
+// overwrite P(t) before PV(t) has read it, and once S(t) is complete PV(t-1)
+// is too.
 // Every wait is bounded (counted polls with a suspend hint); a wait that gives
 // up sets the workspace status word and an abort flag, and the CTA finishes
 // without further work.
@@ -42,30 +51,34 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRows = 128;        // packed query rows per tile
+constexpr int kSub = 2;           // 128-row subtiles per query tile
+constexpr int kRows = 128;        // rows per subtile (M)
 constexpr int kKvTile = 128;      // KV tokens per tile
 constexpr int kD = 128;           // head dim
-constexpr int kKvStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalf = 16384;      // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kTile = 2 * kHalf;  // [128 rows][128 bf16]
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
-constexpr int kOffV = kOffK + kKvStages * kTile;
-constexpr int kOffP = kOffV + kKvStages * kTile;
-constexpr int kOffBar = kOffP + kTile;
-enum Bar { kQFull = 0, kQEmpty, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull, kSFree, kPFull, kODone, kOFree, kNumBars };
+constexpr int kOffQ = 0;                        // kSub tiles
+constexpr int kOffK = kOffQ + kSub * kTile;     // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;        // 2 stages
+constexpr int kOffBar = kOffV + 2 * kTile;
+enum Bar {
+    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+    kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
+};
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 227 * 1024, "prefill tiles exceed shared memory");
 
-constexpr uint32_t kTmemCols = 256;  // S at [0, 128), O at [128, 256)
+// TMEM columns: S0 (P0 over its first 64 columns) | S1 (P1) | O0 | O1
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitHintNs = 100000;
 constexpr uint32_t kWaitPolls = 10000;  // about 1 s
 constexpr int kStatusWait = 0x201;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 struct PrefillParams {
     const uint8_t *ws;
@@ -96,6 +109,12 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctx &c, uint32_t bar, uint32
     return __all_sync(0xffffffffu, wait_bar(c, bar, parity));
 }
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -114,17 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + p.off_status)};
 
     if (tid == 0) {
-        mbar_init(bar(kQFull), 1);
-        mbar_init(bar(kQEmpty), 1);
-        mbar_init(bar(kKvFull0), 1);
-        mbar_init(bar(kKvFull1), 1);
-        mbar_init(bar(kKvEmpty0), 1);
-        mbar_init(bar(kKvEmpty1), 1);
-        mbar_init(bar(kSFull), 1);
-        mbar_init(bar(kSFree), 128);
-        mbar_init(bar(kPFull), 128);
-        mbar_init(bar(kODone), 1);
-        mbar_init(bar(kOFree), 128);
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool softmax_arrivals = i == kPFull0 || i == kPFull1 || i == kOFree0 || i == kOFree1;
+            mbar_init(bar(i), softmax_arrivals ? 128 : 1);
+        }
         *ctx.abort_flag = 0;
         fence_barrier_init();
     }
@@ -142,116 +154,159 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int g = p.g;
+    const int pos_per_sub = kRows / g;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
-        int q_cnt = 0, kv_cnt = 0;
-        for (int it = it0; it < it1 && !*ctx.abort_flag; ++it) {
+        int q_cnt = 0, j = 0;  // j: KV tiles issued so far
+        bool ok = true;
+        for (int it = it0; it < it1 && ok; ++it) {
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
             const int nt = (len + kKvTile - 1) / kKvTile;
             if (nt == 0) continue;
-            if (!wait_bar_warp(ctx, bar(kQEmpty), (q_cnt & 1) ^ 1)) break;
+            if (!(ok = wait_bar_warp(ctx, bar(kQEmpty), (q_cnt & 1) ^ 1))) break;
             ++q_cnt;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(kQFull), kTile);
-                tma_load_3d(sb + kOffQ, &tq, bar(kQFull), 0, w.kv_head * g, w.q_tok0);
-                tma_load_3d(sb + kOffQ + kHalf, &tq, bar(kQFull), 64, w.kv_head * g, w.q_tok0);
+                mbar_arrive_expect_tx(bar(kQFull), kSub * kTile);
+#pragma unroll
+                for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sb + kOffQ + sub * kTile + h * kHalf, &tq, bar(kQFull), h * 64, w.kv_head * g,
+                                    w.q_tok0 + sub * pos_per_sub);
             }
-            bool ok = true;
-            for (int t = 0; t < nt && ok; ++t, ++kv_cnt) {
+            for (int t = 0; t < nt; ++t, ++j) {
                 const int tok0 = w.kv_start + t * kKvTile;
                 const int valid = min(kKvTile, len - t * kKvTile);
                 const int nseg = (valid + p.box_rows - 1) / p.box_rows;
                 int page = 0;
                 if (lane < nseg) page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
-                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
-                ok = wait_bar_warp(ctx, bar(kKvEmpty0 + stage), (round & 1) ^ 1);
-                if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kKvFull0 + stage), (uint32_t)nseg * p.box_rows * 128 * 4);
+                const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
+                const uint32_t seg = (uint32_t)lane * p.box_rows * 128;
+                const uint32_t bytes = (uint32_t)nseg * p.box_rows * 128 * 2;
+                const int stage = j & 1, round = j >> 1;
+                if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull0 + stage), bytes);
                 __syncwarp();
                 if (lane < nseg) {
-                    const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
-                    const uint32_t off = (uint32_t)lane * p.box_rows * 128;
-                    const uint32_t dk = sb + kOffK + stage * kTile + off, dv = sb + kOffV + stage * kTile + off;
-                    tma_load_3d(dk, &tk, bar(kKvFull0 + stage), 0, w.kv_head, row0);
-                    tma_load_3d(dk + kHalf, &tk, bar(kKvFull0 + stage), 64, w.kv_head, row0);
-                    tma_load_3d(dv, &tv, bar(kKvFull0 + stage), 0, w.kv_head, row0);
-                    tma_load_3d(dv + kHalf, &tv, bar(kKvFull0 + stage), 64, w.kv_head, row0);
+                    const uint32_t d = sb + kOffK + stage * kTile + seg;
+                    tma_load_3d(d, &tk, bar(kKFull0 + stage), 0, w.kv_head, row0);
+                    tma_load_3d(d + kHalf, &tk, bar(kKFull0 + stage), 64, w.kv_head, row0);
+                }
+                if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + stage), (round & 1) ^ 1))) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + stage), bytes);
+                __syncwarp();
+                if (lane < nseg) {
+                    const uint32_t d = sb + kOffV + stage * kTile + seg;
+                    tma_load_3d(d, &tv, bar(kVFull0 + stage), 0, w.kv_head, row0);
+                    tma_load_3d(d + kHalf, &tv, bar(kVFull0 + stage), 64, w.kv_head, row0);
                 }
             }
-            if (!ok) break;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         constexpr uint32_t id_s = idesc_bf16_f32(kRows, kKvTile, false, false);
         constexpr uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
-        const uint32_t tS = tmem, tO = tmem + 128;
-        int q_cnt = 0, kv_cnt = 0, s_cnt = 0, p_cnt = 0, done = 0;
+        int q_cnt = 0, j = 0, p_cnt0 = 0, p_cnt1 = 0, done = 0;
         bool ok = true;
+        // S(sub) = Q(sub) K(stage)^T
+        auto issue_s = [&](int sub, int stage) {
+            if (lane == 0) {
+                const uint32_t sq = sb + kOffQ + sub * kTile, sk = sb + kOffK + stage * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + sub * 128, smem_desc_sw128(sq + o, 16, 1024), smem_desc_sw128(sk + o, 16, 1024),
+                                id_s, kk > 0);
+                }
+                mma_commit(bar(kSFull0 + sub));
+            }
+            __syncwarp();
+        };
+        // O(sub) += P(sub) V(stage), P from TMEM
+        auto issue_pv = [&](int sub, int stage, bool acc) {
+            if (lane == 0) {
+                const uint32_t sv = sb + kOffV + stage * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kKvTile / 16; ++kk)
+                    mma_bf16_ts(tmem + 256 + sub * 128, tmem + sub * 128 + kk * 8,
+                                smem_desc_sw128(sv + kk * 16 * 128, kHalf, 1024), id_pv, acc || kk > 0);
+            }
+            __syncwarp();
+        };
+        auto commit = [&](int b) {
+            if (lane == 0) mma_commit(bar(b));
+            __syncwarp();
+        };
+        // One subtile's turn in tile t: PV(t), then S(t+1).
+        auto turn = [&](int sub, int p_count, int t, int nt, int st, int stn, int rdn) -> bool {
+            if (!wait_bar_warp(ctx, bar(kPFull0 + sub), p_count & 1)) return false;
+            if (t == 0 && done > 0 && !wait_bar_warp(ctx, bar(kOFree0 + sub), (done - 1) & 1)) return false;
+            tc_fence_after();
+            issue_pv(sub, st, t > 0);
+            if (t == nt - 1) commit(kODone0 + sub);
+            if (sub == 1) commit(kVEmpty0 + st);
+            if (t + 1 < nt) {
+                if (sub == 0 && !wait_bar_warp(ctx, bar(kKFull0 + stn), rdn & 1)) return false;
+                tc_fence_after();
+                issue_s(sub, stn);
+                if (sub == 1) {
+                    commit(kKEmpty0 + stn);
+                    if (t + 1 == nt - 1) commit(kQEmpty);
+                }
+            }
+            return true;
+        };
         for (int it = it0; it < it1 && ok; ++it) {
             const bsp_work_item w = items[it];
             const int nt = (w.kv_end - w.kv_start + kKvTile - 1) / kKvTile;
             if (nt == 0) continue;
             if (!(ok = wait_bar_warp(ctx, bar(kQFull), q_cnt & 1))) break;
             ++q_cnt;
-            for (int t = 0; t < nt; ++t, ++kv_cnt) {
-                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
-                if (!(ok = wait_bar_warp(ctx, bar(kKvFull0 + stage), round & 1))) break;
-                if (!(ok = wait_bar_warp(ctx, bar(kSFree), (s_cnt & 1) ^ 1))) break;
-                ++s_cnt;
-                tc_fence_after();
-                const uint32_t sK = sb + kOffK + stage * kTile, sV = sb + kOffV + stage * kTile;
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        mma_bf16_ss(tS, smem_desc_sw128(sb + kOffQ + o, 16, 1024), smem_desc_sw128(sK + o, 16, 1024),
-                                    id_s, kk > 0);
-                    }
-                    mma_commit(bar(kSFull));
-                    if (t == nt - 1) mma_commit(bar(kQEmpty));
-                }
-                __syncwarp();
-                if (!(ok = wait_bar_warp(ctx, bar(kPFull), p_cnt & 1))) break;
-                ++p_cnt;
-                if (t == 0 && done > 0 && !(ok = wait_bar_warp(ctx, bar(kOFree), (done - 1) & 1))) break;
-                tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                        const uint32_t po = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        mma_bf16_ss(tO, smem_desc_sw128(sb + kOffP + po, 16, 1024),
-                                    smem_desc_sw128(sV + kk * 16 * 128, kHalf, 1024), id_pv, (t > 0 || kk > 0));
-                    }
-                    mma_commit(bar(kODone));
-                    mma_commit(bar(kKvEmpty0 + stage));
-                }
-                __syncwarp();
+            const int j0 = j;
+            // prologue: S0(0), S1(0)
+            if (!(ok = wait_bar_warp(ctx, bar(kKFull0 + (j0 & 1)), (j0 >> 1) & 1))) break;
+            tc_fence_after();
+            issue_s(0, j0 & 1);
+            issue_s(1, j0 & 1);
+            commit(kKEmpty0 + (j0 & 1));
+            if (nt == 1) commit(kQEmpty);
+            for (int t = 0; t < nt && ok; ++t) {
+                const int jt = j0 + t, st = jt & 1, rd = jt >> 1;
+                const int jn = jt + 1, stn = jn & 1, rdn = jn >> 1;
+                if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + st), rd & 1))) break;
+                if (!(ok = turn(0, p_cnt0, t, nt, st, stn, rdn))) break;
+                ++p_cnt0;
+                if (!(ok = turn(1, p_cnt1, t, nt, st, stn, rdn))) break;
+                ++p_cnt1;
             }
+            j = j0 + nt;
             ++done;
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int q4 = warp & 3;
-        const int r = q4 * 32 + lane;
+        const int sub = (warp - 2) >> 2;       // warps 2-5: subtile 0, warps 6-9: subtile 1
+        const int q4 = warp & 3;               // TMEM lane quarter of this warp
+        const int r = q4 * 32 + lane;          // row within the subtile
+        const int rt = sub * kRows + r;        // row within the 256-row tile
         const uint32_t tl = (uint32_t)(q4 * 32) << 16;
-        const uint32_t tS = tmem + tl, tO = tmem + tl + 128;
+        const uint32_t tS = tmem + tl + sub * 128, tO = tmem + tl + 256 + sub * 128;
         float *plse = reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse);
         float *po = reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_po);
-        int s_cnt = 0, pv_cnt = 0, kv_cnt = 0;
+        int s_cnt = 0, o_cnt = 0, j = 0;
         bool ok = true;
         for (int it = it0; it < it1 && ok; ++it) {
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
             const int nt = (len + kKvTile - 1) / kKvTile;
-            const int pos = w.pos0 + r / g;
+            const int pos = w.pos0 + rt / g;
             const int lim = p.causal ? pos + w.kv_len - w.qo_len : INT_MAX;  // key j allowed iff j <= lim
-            float m = -INFINITY, l = 0.f;
-            for (int t = 0; t < nt; ++t, ++kv_cnt) {
+            float m = -INFINITY, l = 0.f;  // m: reference maximum (scaled, base 2)
+            for (int t = 0; t < nt; ++t, ++j) {
                 const int tok0 = w.kv_start + t * kKvTile;
                 const int valid = min(kKvTile, len - t * kKvTile);
-                if (!(ok = wait_bar_warp(ctx, bar(kSFull), s_cnt & 1))) break;
+                if (!(ok = wait_bar_warp(ctx, bar(kSFull0 + sub), s_cnt & 1))) break;
                 ++s_cnt;
                 tc_fence_after();
                 float sv[kKvTile];
@@ -263,55 +318,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
                 }
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar(kSFree));
-                // scale, mask, running max
+                const bool full = valid == kKvTile && tok0 + kKvTile - 1 <= lim;
                 float mx = -INFINITY;
+                if (full) {
 #pragma unroll
-                for (int c = 0; c < kKvTile; ++c) {
-                    const bool allowed = c < valid && tok0 + c <= lim;
-                    sv[c] = allowed ? sv[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
+                    for (int c = 0; c < kKvTile; ++c) mx = fmaxf(mx, sv[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kKvTile; ++c) {
+                        sv[c] = (c < valid && tok0 + c <= lim) ? sv[c] : -INFINITY;
+                        mx = fmaxf(mx, sv[c]);
+                    }
                 }
-                const float mn = fmaxf(m, mx);
-                const float ref = mn == -INFINITY ? 0.f : mn;
-                const float alpha = exp2f(m - ref);
+                const float mxs = mx * p.scale_log2;                 // scale > 0 keeps the order
+                const bool move = mxs > m + kRescaleThreshold;       // false for an all-masked row
+                const float alpha = move ? ex2(m - mxs) : 1.f;       // 0 when m was -inf
+                if (move) {
+                    l *= alpha;
+                    m = mxs;
+                }
+                const float ref = m == -INFINITY ? 0.f : m;
                 float sum = 0.f;
 #pragma unroll
                 for (int c = 0; c < kKvTile; ++c) {
-                    sv[c] = exp2f(sv[c] - ref);
+                    sv[c] = ex2(fmaf(sv[c], p.scale_log2, -ref));
                     sum += sv[c];
                 }
-                l = l * alpha + sum;
-                m = mn;
-                const int stage = kv_cnt % kKvStages, round = kv_cnt / kKvStages;
-                if (valid < kKvTile) {
-                    // rows past the chunk end: zero V so that P = 0 meets finite values
-                    if (!(ok = wait_bar_warp(ctx, bar(kKvFull0 + stage), round & 1))) break;
-                    if (r >= valid) {
-                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + stage * kTile + r * 128);
-                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + stage * kTile + kHalf + r * 128);
+                l += sum;
+                // P (bf16 pairs) over the first 64 columns of S
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                // the previous PV must be done before P is overwritten and O rescaled
-                if (t > 0) {
-                    if (!(ok = wait_bar_warp(ctx, bar(kODone), pv_cnt & 1))) break;
-                    ++pv_cnt;
-                    tc_fence_after();
-                }
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int ch = 0; ch < kKvTile / 8; ++ch) {
-                    uint4 u;
-                    u.x = dev::pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-                    u.y = dev::pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-                    u.z = dev::pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-                    u.w = dev::pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-                    const int half = ch >> 3, kc = ch & 7;
-                    *reinterpret_cast<uint4 *>(smem + kOffP + half * kHalf + r * 128 + ((kc ^ (r & 7)) << 4)) = u;
+                    for (int i = 0; i < 32; ++i) pk[i] = dev::pack_bf16(sv[c * 64 + 2 * i], sv[c * 64 + 2 * i + 1]);
+                    tmem_st32_u(tS + c * 32, pk);
                 }
-                if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O rescale when the reference moved (PV(t-1) is complete: S(t) is)
+                if (t > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
                     for (int c = 0; c < kD / 32; ++c) {
                         float v[32];
@@ -321,25 +364,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) v[i] *= alpha;
                         tmem_st32(tO + c * 32, v);
                     }
-                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();
+                if (sub == 0 && valid < kKvTile) {
+                    // rows past the chunk end: zero V so that P = 0 meets finite values
+                    if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + (j & 1)), (j >> 1) & 1))) break;
+                    if (r >= valid) {
+                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + (j & 1) * kTile + r * 128);
+                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + (j & 1) * kTile + kHalf + r * 128);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
                 tc_fence_before();
-                mbar_arrive(bar(kPFull));
+                mbar_arrive(bar(kPFull0 + sub));
             }
             if (!ok) break;
             // ---- epilogue: O / l, LSE; final output or partial state ----
             if (nt > 0) {
-                if (!(ok = wait_bar_warp(ctx, bar(kODone), pv_cnt & 1))) break;
-                ++pv_cnt;
+                if (!(ok = wait_bar_warp(ctx, bar(kODone0 + sub), o_cnt & 1))) break;
+                ++o_cnt;
                 tc_fence_after();
             }
-            const bool row_ok = r < w.n_pos * g;
+            const bool row_ok = rt < w.n_pos * g;
             const bool has = l > 0.f;
             const float inv = has ? 1.f / l : 0.f;
             const float lse_v = has ? (m + log2f(l)) * dev::kLn2 : -INFINITY;
-            const size_t orow = (size_t)(w.q_tok0 + r / g) * p.H_qo + (size_t)w.kv_head * g + (r % g);
-            const size_t prow = (size_t)w.slot * p.tile_rows + r;
+            const size_t orow = (size_t)(w.q_tok0 + rt / g) * p.H_qo + (size_t)w.kv_head * g + (rt % g);
+            const size_t prow = (size_t)w.slot * p.tile_rows + rt;
 #pragma unroll
             for (int c = 0; c < kD / 32; ++c) {
                 float v[32];
@@ -379,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (nt > 0) {
                 tc_fence_before();
-                mbar_arrive(bar(kOFree));
+                mbar_arrive(bar(kOFree0 + sub));
             }
         }
     }
@@ -445,7 +498,8 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     if (P.head_dim != kD) return fail(BSP_ERR_UNSUPPORTED, "prefill supports head_dim 128 only");
     if (P.page_size < 8 || (P.page_size & (P.page_size - 1)) != 0)
         return fail(BSP_ERR_UNSUPPORTED, "prefill needs page_size a power of two >= 8");
-    if (plan->tile_rows != kRows || kRows % g != 0) return fail(BSP_ERR_UNSUPPORTED, "prefill needs 128 % g == 0");
+    if (plan->tile_rows != kSub * kRows || kRows % g != 0)
+        return fail(BSP_ERR_UNSUPPORTED, "prefill needs 256-row tiles and 128 % g == 0");
     if (num_pages * (int64_t)P.page_size > INT32_MAX) return fail(BSP_ERR_UNSUPPORTED, "KV pool beyond 2^31 rows");
 
     CUtensorMap tq, tk, tv;

@@ -80,7 +80,7 @@ typedef struct CUstream_st *bsp_stream_t; /* same type as cudaStream_t */
 #define BSP_DTYPE_F32  1
 
 #define BSP_MODE_DECODE  0 /* query tile = the g fused heads of one position */
-#define BSP_MODE_PREFILL 1 /* query tile = 128 packed rows                   */
+#define BSP_MODE_PREFILL 1 /* query tile = 256 packed rows (two MMA subtiles) */
 
 /* Static problem description: what stays fixed across steps and layers. */
 typedef struct bsp_problem {
@@ -169,7 +169,7 @@ size_t bsp_host_staging_size(const bsp_problem *problem, const bsp_capacity *cap
  * Plan one step (FlashInfer 原理 overview, ⑨; technical review §6.1-6.2
  * Algorithm 2; engineering walkthrough §VIII.2, §VIII.5):
  *   query tiles of T_q packed rows (decode: g rows, one position; prefill:
- *   128 rows), W = sum over (tile, kv head) of kv_len, chunk length
+ *   256 rows), W = sum over (tile, kv head) of kv_len, chunk length
  *   L = ceil(W / C) rounded up to a page, chunks of each tile's visible range
  *   sorted longest first (ties by (b, tile, kv_head, kv_start)), assigned to
  *   CTAs by a min-heap on (cost, cta), cost += alpha * positions + beta *
@@ -222,7 +222,7 @@ int bsp_decode_run(const bsp_plan_info *plan, const void *q, const void *k_pages
                    void *o, float *lse, void *workspace, bsp_stream_t stream);
 
 /*
- * Prefill run: ragged queries, tiles of 128 packed rows (positions x g heads,
+ * Prefill run: ragged queries, tiles of 256 packed rows (positions x g heads,
  * technical review eq 3) against KV tiles gathered page by page into shared
  * memory, QK^T and PV on the tensor cores (sparse gather, dense compute:
  * overview ⑥, walkthrough §IV.2 and §V.4), then the merge of split outputs.

@@ -32,7 +32,7 @@ def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alph
     info, queue, items, merges = bsp.plan_host(prob, cap, kv_indptr, last,
                                                None if mode == bsp.BSP_MODE_DECODE and np.all(qo_lens == 1) else qo_indptr,
                                                alpha, beta)
-    tile = g if mode == bsp.BSP_MODE_DECODE else 128
+    tile = g if mode == bsp.BSP_MODE_DECODE else 256
     ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta)
     return info, queue, items, merges, ref, qo_indptr, kv_indptr
 
