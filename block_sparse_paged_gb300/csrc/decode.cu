@@ -25,7 +25,7 @@
 //   - output: the final (O, LSE) when the item is its output's only chunk,
 //     else an fp32 partial state in the workspace slot the plan assigned
 //     (overview ⑨, write-through of unsplit requests).
-//   - every wait is bounded (about 1 s of polls); a wait that gives up sets the workspace
+//   - every wait is a bounded spin (SM clock cycles); a wait that gives up sets the workspace
 //     status word and an abort flag the other warps see, and the CTA returns.
 // Reduction kernel: the reduction map's slots of each split output, merged in
 // ascending order with a common maximum (technical review eq 6), no atomics.
@@ -49,8 +49,7 @@ constexpr int kConsumers = 4;
 constexpr int kWsThreads = 32 * (kConsumers + 2);
 constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per consumer warp)
 constexpr int kStages = 5;
-constexpr uint32_t kWaitHintNs = 100000;     // one poll sleeps up to 100 us unless the phase completes
-constexpr uint32_t kWaitPolls = 10000;       // so a wait gives up after about 1 s: a fault, not a stall
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 
 template <int D>
 struct DecodeLayout {
@@ -85,12 +84,11 @@ constexpr int kStatusMergeWait = 0x103;
 // Bounded mbarrier wait that also gives up as soon as another warp aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
                                               int code) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i) {
-        if (sm100::mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
-        if (*abort_flag) return false;
+    if (sm100::mbar_wait_spin(bar, parity, kWaitLimitCycles, abort_flag)) return true;
+    if (!*abort_flag) {
+        *abort_flag = 1;
+        atomicCAS(status, 0, code);
     }
-    *abort_flag = 1;
-    atomicCAS(status, 0, code);
     return false;
 }
 

@@ -33,7 +33,7 @@
 // rescaled only then. MMAs of the CTA execute in issue order, so S(t+1) cannot
 // overwrite P(t) before PV(t) has read it, and once S(t) is complete PV(t-1)
 // is too.
-// Every wait is bounded (counted polls with a suspend hint); a wait that gives
+// Every wait is a bounded spin (SM clock cycles); a wait that gives
 // up sets the workspace status word and an abort flag, and the CTA finishes
 // without further work.
 #include <cuda.h>
@@ -75,8 +75,7 @@ static_assert(kSmemBytes <= 227 * 1024, "prefill tiles exceed shared memory");
 
 // TMEM columns: S0 (P0 over its first 64 columns) | S1 (P1) | O0 | O1
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kWaitHintNs = 100000;
-constexpr uint32_t kWaitPolls = 10000;  // about 1 s
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 constexpr int kStatusWait = 0x201;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
@@ -96,10 +95,7 @@ struct Ctx {
 };
 
 __device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i) {
-        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
-        if (*c.abort_flag) return false;
-    }
+    if (mbar_wait_spin(bar, parity, kWaitLimitCycles, c.abort_flag)) return true;
     *c.abort_flag = 1;
     atomicCAS(c.status, 0, kStatusWait);
     return false;
@@ -319,17 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_ld();
                 const bool full = valid == kKvTile && tok0 + kKvTile - 1 <= lim;
-                float mx = -INFINITY;
-                if (full) {
+                if (!full) {
 #pragma unroll
-                    for (int c = 0; c < kKvTile; ++c) mx = fmaxf(mx, sv[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kKvTile; ++c) {
-                        sv[c] = (c < valid && tok0 + c <= lim) ? sv[c] : -INFINITY;
-                        mx = fmaxf(mx, sv[c]);
-                    }
+                    for (int c = 0; c < kKvTile; ++c) sv[c] = (c < valid && tok0 + c <= lim) ? sv[c] : -INFINITY;
                 }
+                // row maximum with 8 independent partial maxima (short dependency chains)
+                float pm[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pm[i] = sv[i];
+#pragma unroll
+                for (int c = 8; c < kKvTile; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                 const float mxs = mx * p.scale_log2;                 // scale > 0 keeps the order
                 const bool move = mxs > m + kRescaleThreshold;       // false for an all-masked row
                 const float alpha = move ? ex2(m - mxs) : 1.f;       // 0 when m was -inf
@@ -338,13 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = mxs;
                 }
                 const float ref = m == -INFINITY ? 0.f : m;
-                float sum = 0.f;
+                float ps[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ps[i] = 0.f;
 #pragma unroll
                 for (int c = 0; c < kKvTile; ++c) {
                     sv[c] = ex2(fmaf(sv[c], p.scale_log2, -ref));
-                    sum += sv[c];
+                    ps[c & 7] += sv[c];
                 }
-                l += sum;
+                l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 // P (bf16 pairs) over the first 64 columns of S
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {

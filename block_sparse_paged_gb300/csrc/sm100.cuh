@@ -46,11 +46,28 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 // Bounded wait: at most `polls` sleeps of about `hint_ns` each (the bound is
-// polls * hint_ns plus overhead). Returns false when the wait gave up.
+// polls * hint_ns plus overhead). Returns false when the wait gave up. A
+// sleeping waiter can wake well after the phase completes, so this is for
+// cold paths; hot paths use mbar_wait_spin.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t polls, uint32_t hint_ns) {
     for (uint32_t i = 0; i < polls; ++i)
         if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
     return false;
+}
+// Bounded spin: try_wait without a suspend hint until the phase completes,
+// `*abort_flag` becomes nonzero, or `limit_cycles` SM clock cycles pass (both
+// checked every 256 polls). Returns false when the wait gave up.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, long long limit_cycles,
+                                               const volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > limit_cycles) return false;
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
