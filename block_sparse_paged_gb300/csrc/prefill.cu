@@ -105,6 +105,25 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctx &c, uint32_t bar, uint32
     return __all_sync(0xffffffffu, wait_bar(c, bar, parity));
 }
 
+// Paired fp32 arithmetic (one instruction for two elements).
+__device__ __forceinline__ void fma2_bcast(float &d0, float &d1, float a0, float a1, float b, float c) {
+    asm("{ .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n mov.b64 rc, {%5, %5};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
+    asm("{ .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(d0), "f"(d1), "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -319,14 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kKvTile; ++c) sv[c] = (c < valid && tok0 + c <= lim) ? sv[c] : -INFINITY;
                 }
-                // row maximum with 8 independent partial maxima (short dependency chains)
+                // row maximum: 8 independent chains of 3-input maxima
                 float pm[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pm[i] = sv[i];
+                for (int i = 0; i < 8; ++i) pm[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
 #pragma unroll
-                for (int c = 8; c < kKvTile; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                for (int c = 16; c < kKvTile; c += 2) pm[(c >> 1) & 7] = max3(pm[(c >> 1) & 7], sv[c], sv[c + 1]);
+                const float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
                 const float mxs = mx * p.scale_log2;                 // scale > 0 keeps the order
                 const bool move = mxs > m + kRescaleThreshold;       // false for an all-masked row
                 const float alpha = move ? ex2(m - mxs) : 1.f;       // 0 when m was -inf
@@ -339,9 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) ps[i] = 0.f;
 #pragma unroll
-                for (int c = 0; c < kKvTile; ++c) {
-                    sv[c] = ex2(fmaf(sv[c], p.scale_log2, -ref));
-                    ps[c & 7] += sv[c];
+                for (int c = 0; c < kKvTile; c += 2) {
+                    fma2_bcast(sv[c], sv[c + 1], sv[c], sv[c + 1], p.scale_log2, -ref);
+                    sv[c] = ex2(sv[c]);
+                    sv[c + 1] = ex2(sv[c + 1]);
+                    const int a = (c >> 1) & 3;
+                    add2(ps[2 * a], ps[2 * a + 1], sv[c], sv[c + 1]);
                 }
                 l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 // P (bf16 pairs) over the first 64 columns of S
