@@ -15,9 +15,9 @@
 // the page table only supplies the copy's row coordinate. The 256 query rows
 // are two 128-row MMA subtiles that share every K and V tile. One CTA per SM,
 // persistent over its plan queue, ten warps:
-//   warp 0      TMA: both Q subtiles of the item, then K and V tiles into two
-//               separate 2-stage rings (K is released after the second S, V
-//               after the second PV)
+//   warp 0      TMA: both Q subtiles of the item, then K and V tiles into a
+//               2-stage K ring and a 3-stage V ring (K is released after the
+//               second S, V after the second PV)
 //   warp 1      TMEM owner and MMA issuer, in the order
 //               S0(0) S1(0) | PV0(t) S0(t+1) PV1(t) S1(t+1) | ...
 //               S = Q K^T (M 128, N 128, K 128) into TMEM; P (bf16) is written
@@ -59,13 +59,15 @@ constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalf = 16384;      // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kTile = 2 * kHalf;  // [128 rows][128 bf16]
 
-constexpr int kOffQ = 0;                        // kSub tiles
-constexpr int kOffK = kOffQ + kSub * kTile;     // 2 stages
-constexpr int kOffV = kOffK + 2 * kTile;        // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTile;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;  // V is released only after the second PV: one more stage hides its refill
+constexpr int kOffQ = 0;                          // kSub tiles
+constexpr int kOffK = kOffQ + kSub * kTile;       // kKStages tiles
+constexpr int kOffV = kOffK + kKStages * kTile;   // kVStages tiles
+constexpr int kOffBar = kOffV + kVStages * kTile;
 enum Bar {
-    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-    kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
+    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1,
+    kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -209,25 +211,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(d, &tk, bar(kKFull0 + stage), 0, w.kv_head, row0);
                     tma_load_3d(d + kHalf, &tk, bar(kKFull0 + stage), 64, w.kv_head, row0);
                 }
-                if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + stage), (round & 1) ^ 1))) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + stage), bytes);
+                const int vst = j % kVStages, vrd = j / kVStages;
+                if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + vst), bytes);
                 __syncwarp();
                 if (lane < nseg) {
-                    const uint32_t d = sb + kOffV + stage * kTile + seg;
-                    tma_load_3d(d, &tv, bar(kVFull0 + stage), 0, w.kv_head, row0);
-                    tma_load_3d(d + kHalf, &tv, bar(kVFull0 + stage), 64, w.kv_head, row0);
+                    const uint32_t d = sb + kOffV + vst * kTile + seg;
+                    tma_load_3d(d, &tv, bar(kVFull0 + vst), 0, w.kv_head, row0);
+                    tma_load_3d(d + kHalf, &tv, bar(kVFull0 + vst), 64, w.kv_head, row0);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        constexpr uint32_t id_s = idesc_bf16_f32(kRows, kKvTile, false, false);
-        constexpr uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
-        int q_cnt = 0, j = 0, p_cnt0 = 0, p_cnt1 = 0, done = 0;
-        bool ok = true;
-        // S(sub) = Q(sub) K(stage)^T
-        auto issue_s = [&](int sub, int stage) {
-            if (lane == 0) {
+        // One thread issues everything: between MMA groups the tensor pipe
+        // drains, so every cycle spent on warp votes, redundant fences or index
+        // arithmetic here is idle tensor time. The only fence needed is after
+        // the P barrier (P arrives through tcgen05.st from other threads); K, V
+        // and Q arrive through TMA (async proxy) with their mbarriers.
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(kRows, kKvTile, false, false);
+            constexpr uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
+            int q_cnt = 0, p_cnt0 = 0, p_cnt1 = 0, done = 0;
+            int kst = 0, kph = 0;  // K ring position of the next tile: stage, phase
+            int vst = 0, vph = 0;  // V ring position of the next tile
+            bool ok = true;
+            auto wait1 = [&](uint32_t b, uint32_t parity) -> bool {
+                if (mbar_wait_spin(b, parity, kWaitLimitCycles, ctx.abort_flag)) return true;
+                *ctx.abort_flag = 1;
+                atomicCAS(ctx.status, 0, kStatusWait);
+                return false;
+            };
+            auto issue_s = [&](int sub, int stage) {
                 const uint32_t sq = sb + kOffQ + sub * kTile, sk = sb + kOffK + stage * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
@@ -236,69 +251,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 id_s, kk > 0);
                 }
                 mma_commit(bar(kSFull0 + sub));
-            }
-            __syncwarp();
-        };
-        // O(sub) += P(sub) V(stage), P from TMEM
-        auto issue_pv = [&](int sub, int stage, bool acc) {
-            if (lane == 0) {
+            };
+            auto issue_pv = [&](int sub, int stage, bool acc) {
                 const uint32_t sv = sb + kOffV + stage * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk)
                     mma_bf16_ts(tmem + 256 + sub * 128, tmem + sub * 128 + kk * 8,
                                 smem_desc_sw128(sv + kk * 16 * 128, kHalf, 1024), id_pv, acc || kk > 0);
-            }
-            __syncwarp();
-        };
-        auto commit = [&](int b) {
-            if (lane == 0) mma_commit(bar(b));
-            __syncwarp();
-        };
-        // One subtile's turn in tile t: PV(t), then S(t+1).
-        auto turn = [&](int sub, int p_count, int t, int nt, int st, int stn, int rdn) -> bool {
-            if (!wait_bar_warp(ctx, bar(kPFull0 + sub), p_count & 1)) return false;
-            if (t == 0 && done > 0 && !wait_bar_warp(ctx, bar(kOFree0 + sub), (done - 1) & 1)) return false;
-            tc_fence_after();
-            issue_pv(sub, st, t > 0);
-            if (t == nt - 1) commit(kODone0 + sub);
-            if (sub == 1) commit(kVEmpty0 + st);
-            if (t + 1 < nt) {
-                if (sub == 0 && !wait_bar_warp(ctx, bar(kKFull0 + stn), rdn & 1)) return false;
-                tc_fence_after();
-                issue_s(sub, stn);
-                if (sub == 1) {
-                    commit(kKEmpty0 + stn);
-                    if (t + 1 == nt - 1) commit(kQEmpty);
+            };
+            for (int it = it0; it < it1 && ok; ++it) {
+                const int nt = (items[it].kv_end - items[it].kv_start + kKvTile - 1) / kKvTile;
+                if (nt == 0) continue;
+                if (!(ok = wait1(bar(kQFull), q_cnt & 1))) break;
+                ++q_cnt;
+                // prologue: S0(0), S1(0) on K tile 0 of the item
+                if (!(ok = wait1(bar(kKFull0 + kst), kph))) break;
+                issue_s(0, kst);
+                issue_s(1, kst);
+                mma_commit(bar(kKEmpty0 + kst));
+                if (nt == 1) mma_commit(bar(kQEmpty));
+                if (++kst == kKStages) { kst = 0; kph ^= 1; }
+                for (int t = 0; t < nt && ok; ++t) {
+                    if (!(ok = wait1(bar(kVFull0 + vst), vph))) break;
+                    const bool more = t + 1 < nt;
+                    // subtile 0: PV0(t), S0(t+1)
+                    if (!(ok = wait1(bar(kPFull0), p_cnt0 & 1))) break;
+                    ++p_cnt0;
+                    if (t == 0 && done > 0 && !(ok = wait1(bar(kOFree0), (done - 1) & 1))) break;
+                    tc_fence_after();
+                    issue_pv(0, vst, t > 0);
+                    if (!more) mma_commit(bar(kODone0));
+                    if (more) {
+                        if (!(ok = wait1(bar(kKFull0 + kst), kph))) break;
+                        issue_s(0, kst);
+                    }
+                    // subtile 1: PV1(t), S1(t+1)
+                    if (!(ok = wait1(bar(kPFull1), p_cnt1 & 1))) break;
+                    ++p_cnt1;
+                    if (t == 0 && done > 0 && !(ok = wait1(bar(kOFree1), (done - 1) & 1))) break;
+                    tc_fence_after();
+                    issue_pv(1, vst, t > 0);
+                    if (!more) mma_commit(bar(kODone1));
+                    mma_commit(bar(kVEmpty0 + vst));
+                    if (++vst == kVStages) { vst = 0; vph ^= 1; }
+                    if (more) {
+                        issue_s(1, kst);
+                        mma_commit(bar(kKEmpty0 + kst));
+                        if (t + 1 == nt - 1) mma_commit(bar(kQEmpty));
+                        if (++kst == kKStages) { kst = 0; kph ^= 1; }
+                    }
                 }
+                ++done;
             }
-            return true;
-        };
-        for (int it = it0; it < it1 && ok; ++it) {
-            const bsp_work_item w = items[it];
-            const int nt = (w.kv_end - w.kv_start + kKvTile - 1) / kKvTile;
-            if (nt == 0) continue;
-            if (!(ok = wait_bar_warp(ctx, bar(kQFull), q_cnt & 1))) break;
-            ++q_cnt;
-            const int j0 = j;
-            // prologue: S0(0), S1(0)
-            if (!(ok = wait_bar_warp(ctx, bar(kKFull0 + (j0 & 1)), (j0 >> 1) & 1))) break;
-            tc_fence_after();
-            issue_s(0, j0 & 1);
-            issue_s(1, j0 & 1);
-            commit(kKEmpty0 + (j0 & 1));
-            if (nt == 1) commit(kQEmpty);
-            for (int t = 0; t < nt && ok; ++t) {
-                const int jt = j0 + t, st = jt & 1, rd = jt >> 1;
-                const int jn = jt + 1, stn = jn & 1, rdn = jn >> 1;
-                if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + st), rd & 1))) break;
-                if (!(ok = turn(0, p_cnt0, t, nt, st, stn, rdn))) break;
-                ++p_cnt0;
-                if (!(ok = turn(1, p_cnt1, t, nt, st, stn, rdn))) break;
-                ++p_cnt1;
-            }
-            j = j0 + nt;
-            ++done;
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
         const int sub = (warp - 2) >> 2;       // warps 2-5: subtile 0, warps 6-9: subtile 1
@@ -388,10 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 if (sub == 0 && valid < kKvTile) {
                     // rows past the chunk end: zero V so that P = 0 meets finite values
-                    if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + (j & 1)), (j >> 1) & 1))) break;
+                    const int vst = j % kVStages, vrd = j / kVStages;
+                    if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + vst), vrd & 1))) break;
                     if (r >= valid) {
-                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + (j & 1) * kTile + r * 128);
-                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + (j & 1) * kTile + kHalf + r * 128);
+                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + vst * kTile + r * 128);
+                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + vst * kTile + kHalf + r * 128);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
                     }
