@@ -15,9 +15,9 @@
 // the page table only supplies the copy's row coordinate. The 256 query rows
 // are two 128-row MMA subtiles that share every K and V tile. One CTA per SM,
 // persistent over its plan queue, ten warps:
-//   warp 0      TMA: both Q subtiles of the item, then K and V tiles into a
-//               2-stage K ring and a 3-stage V ring (K is released after the
-//               second S, V after the second PV)
+//   warp 0      TMA: both Q subtiles of the item, then K and V tiles into two
+//               2-stage rings (K is released after the second S, V after the
+//               second PV)
 //   warp 1      TMEM owner and MMA issuer, in the order
 //               S0(0) S1(0) | PV0(t) S0(t+1) PV1(t) S1(t+1) | ...
 //               S = Q K^T (M 128, N 128, K 128) into TMEM; P (bf16) is written
@@ -26,6 +26,10 @@
 //   warps 2-5   softmax of subtile 0, warps 6-9 softmax of subtile 1: one thread
 //               per row; scale, mask (only on tiles that need it), base-2 online
 //               softmax, P to TMEM, O rescale in TMEM, epilogue O / l and LSE.
+//               O is read out of TMEM at once (freeing it for the next item's
+//               PV); each warp turns its 32 bf16 output rows around in a small
+//               swizzled shared-memory buffer so that its global stores cover
+//               whole 128-byte lines (fp32 partial states are stored directly).
 // While one softmax group works on its S, the tensor core runs the other
 // subtile's PV and next S. The reference maximum of a row is only moved when
 // the running maximum exceeds it by more than 8 (a factor 256): the result is
@@ -60,14 +64,16 @@ constexpr int kHalf = 16384;      // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kTile = 2 * kHalf;  // [128 rows][128 bf16]
 
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;  // V is released only after the second PV: one more stage hides its refill
+constexpr int kVStages = 2;
 constexpr int kOffQ = 0;                          // kSub tiles
 constexpr int kOffK = kOffQ + kSub * kTile;       // kKStages tiles
 constexpr int kOffV = kOffK + kKStages * kTile;   // kVStages tiles
-constexpr int kOffBar = kOffV + kVStages * kTile;
+constexpr int kStgWarp = 32 * 128;                 // per softmax warp: 32 rows x 64 bf16, swizzled
+constexpr int kOffStg = kOffV + kVStages * kTile;  // output staging, 8 warps
+constexpr int kOffBar = kOffStg + 8 * kStgWarp;
 enum Bar {
-    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1,
-    kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
+    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+    kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -409,57 +415,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- epilogue: O / l, LSE; final output or partial state ----
+            // O leaves TMEM first, so that the next item's PV may start while
+            // this one is written out.
+            float ov[kD];
             if (nt > 0) {
                 if (!(ok = wait_bar_warp(ctx, bar(kODone0 + sub), o_cnt & 1))) break;
                 ++o_cnt;
                 tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tO + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[c * 32 + i] = v[i];
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(kOFree0 + sub));
+            } else {
+#pragma unroll
+                for (int i = 0; i < kD; ++i) ov[i] = 0.f;
             }
-            const bool row_ok = rt < w.n_pos * g;
             const bool has = l > 0.f;
             const float inv = has ? 1.f / l : 0.f;
             const float lse_v = has ? (m + log2f(l)) * dev::kLn2 : -INFINITY;
             const size_t orow = (size_t)(w.q_tok0 + rt / g) * p.H_qo + (size_t)w.kv_head * g + (rt % g);
             const size_t prow = (size_t)w.slot * p.tile_rows + rt;
+            const int n_rows = w.n_pos * g;  // real rows of the tile
+            if (w.slot < 0) {
+                // bf16 output through this warp's swizzled staging, 64 columns at a
+                // time: each thread writes its row, then every store instruction
+                // covers four whole 128-byte lines (lane l: row 4i + l/8, chunk l%8)
+                const uint32_t stg = sb + kOffStg + (warp - 2) * kStgWarp;
+                const int cc = lane & 7;
+                const int rt_base = sub * kRows + q4 * 32;
+                unsigned long long orr[8];
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
-                float v[32];
-                if (nt > 0) {
-                    tmem_ld32(tO + c * 32, v);
-                    tmem_wait_ld();
-                } else {
+                for (int i = 0; i < 8; ++i) orr[i] = __shfl_sync(0xffffffffu, (unsigned long long)orow, 4 * i + (lane >> 3));
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                }
-                if (row_ok) {
-                    if (w.slot < 0) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + orow * kD + c * 32);
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 u;
-                            u.x = dev::pack_bf16(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
-                            u.y = dev::pack_bf16(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
-                            u.z = dev::pack_bf16(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
-                            u.w = dev::pack_bf16(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
-                            dst[q] = u;
-                        }
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(po + prow * kD + c * 32);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(v[q * 4] * inv, v[q * 4 + 1] * inv, v[q * 4 + 2] * inv, v[q * 4 + 3] * inv);
+                    for (int q = 0; q < 8; ++q) {
+                        const float *x = ov + h * 64 + q * 8;
+                        st_shared_v4(stg + lane * 128 + ((q ^ (lane & 7)) << 4), dev::pack_bf16(x[0] * inv, x[1] * inv),
+                                     dev::pack_bf16(x[2] * inv, x[3] * inv), dev::pack_bf16(x[4] * inv, x[5] * inv),
+                                     dev::pack_bf16(x[6] * inv, x[7] * inv));
                     }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3);
+                        const uint4 val = ld_shared_v4(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+                        if (rt_base + rr < n_rows)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + orr[i] * kD + h * 64 + cc * 8) =
+                                val;
+                    }
+                    __syncwarp();
                 }
+            } else if (rt < n_rows) {
+                // fp32 partial state: this thread's row is 512 contiguous bytes
+                float4 *dst = reinterpret_cast<float4 *>(po + prow * kD);
+#pragma unroll
+                for (int q = 0; q < kD / 4; ++q)
+                    dst[q] = make_float4(ov[q * 4] * inv, ov[q * 4 + 1] * inv, ov[q * 4 + 2] * inv, ov[q * 4 + 3] * inv);
             }
-            if (row_ok) {
+            if (rt < n_rows) {
                 if (w.slot < 0) {
                     if (p.lse) p.lse[orow] = lse_v;
                 } else {
                     plse[prow] = lse_v;
                 }
-            }
-            if (nt > 0) {
-                tc_fence_before();
-                mbar_arrive(bar(kOFree0 + sub));
             }
         }
     }
