@@ -132,6 +132,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return m;
 }
 
+// A read-only global load issued where it stands (its value is waited for at first use).
+__device__ __forceinline__ int ld_nc_s32(const int *p) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -163,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *ctx.abort_flag = 0;
         fence_barrier_init();
     }
+    // V ring starts zeroed: rows a tile does not copy then always hold finite values
+    for (int i = threadIdx.x; i < kVStages * kTile / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + kOffV)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
@@ -265,9 +276,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ts(tmem + 256 + sub * 128, tmem + sub * 128 + kk * 8,
                                 smem_desc_sw128(sv + kk * 16 * 128, kHalf, 1024), id_pv, acc || kk > 0);
             };
+            // the next item's KV range is read one item ahead (its latency then
+            // overlaps this item's MMAs instead of delaying the next item's first S)
+            int nt_next = (items[it0].kv_end - items[it0].kv_start + kKvTile - 1) / kKvTile;
             for (int it = it0; it < it1 && ok; ++it) {
-                const int nt = (items[it].kv_end - items[it].kv_start + kKvTile - 1) / kKvTile;
-                if (nt == 0) continue;
+                const int nt = nt_next;
+                int ks = 0, ke = 0;
+                if (it + 1 < it1) {
+                    ks = ld_nc_s32(&items[it + 1].kv_start);
+                    ke = ld_nc_s32(&items[it + 1].kv_end);
+                }
+                if (nt == 0) {
+                    nt_next = (ke - ks + kKvTile - 1) / kKvTile;
+                    continue;
+                }
                 if (!(ok = wait1(bar(kQFull), q_cnt & 1))) break;
                 ++q_cnt;
                 // prologue: S0(0), S1(0) on K tile 0 of the item
@@ -308,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ++done;
+                nt_next = (ke - ks + kKvTile - 1) / kKvTile;
             }
         }
         __syncwarp();
@@ -329,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = (len + kKvTile - 1) / kKvTile;
             const int pos = w.pos0 + rt / g;
             const int lim = p.causal ? pos + w.kv_len - w.qo_len : INT_MAX;  // key j allowed iff j <= lim
+            asm volatile("" ::"r"(lim), "r"(len), "r"(w.kv_start));  // loaded before the S wait, not after
             float m = -INFINITY, l = 0.f;  // m: reference maximum (scaled, base 2)
             for (int t = 0; t < nt; ++t, ++j) {
                 const int tok0 = w.kv_start + t * kKvTile;
@@ -398,11 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tmem_wait_st();
-                if (sub == 0 && valid < kKvTile) {
-                    // rows past the chunk end: zero V so that P = 0 meets finite values
+                const int vz_end = min(kKvTile, (valid + p.box_rows - 1) / p.box_rows * p.box_rows);
+                if (sub == 0 && valid < vz_end) {
+                    // rows of the last copied box past the chunk end may hold anything:
+                    // zero them so that P = 0 meets finite values (rows past the box keep
+                    // an earlier tile's finite values, the ring starts zeroed)
                     const int vst = j % kVStages, vrd = j / kVStages;
                     if (!(ok = wait_bar_warp(ctx, bar(kVFull0 + vst), vrd & 1))) break;
-                    if (r >= valid) {
+                    if (r >= valid && r < vz_end) {
                         uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + vst * kTile + r * 128);
                         uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + vst * kTile + kHalf + r * 128);
 #pragma unroll
