@@ -93,7 +93,7 @@ def load():
         "bsp_workspace_size": ([P, C], ctypes.c_size_t),
         "bsp_host_staging_size": ([P, C], ctypes.c_size_t),
         "bsp_plan": ([P, C, i32, vp, vp, vp, i64, i64, vp, vp, ctypes.c_size_t, vp, PI], ctypes.c_int),
-        "bsp_decode_run": ([PI, vp, vp, vp, vp, f32, vp, vp, vp, vp], ctypes.c_int),
+        "bsp_decode_run": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_prefill_run": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_run_attention": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_run_merge_partials": ([PI, vp, vp, vp, vp], ctypes.c_int),

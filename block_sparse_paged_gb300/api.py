@@ -171,7 +171,7 @@ class PagedAttention:
         with torch.cuda.device(dev):
             s = _stream_handle(stream)
             if self.mode == N.BSP_MODE_DECODE:
-                N.check(self.lib.bsp_decode_run(*args, *tail, s))
+                N.check(self.lib.bsp_decode_run(*args, k_pages.shape[0], *tail, s))
             else:
                 N.check(self.lib.bsp_prefill_run(*args, k_pages.shape[0], *tail, s))
         return (out, lse) if return_lse else out

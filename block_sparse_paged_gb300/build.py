@@ -31,7 +31,7 @@ def _flags(src: str) -> list[str]:
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
     if src.endswith(".cu"):
         return common + ARCH + ["-lineinfo", "--expt-relaxed-constexpr", "-Xptxas", "-v" if os.environ.get("BSP_PTXAS_V") else "-O3"]
-    return common + ["-x", "cu"] + ARCH if False else common
+    return common
 
 
 def _sources() -> list[str]:

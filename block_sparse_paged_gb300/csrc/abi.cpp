@@ -62,13 +62,14 @@ extern "C" int bsp_default_num_ctas(int32_t mode, int32_t device, int32_t *num_c
 }
 
 extern "C" int bsp_decode_run(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
-                              const int32_t *kv_indices, float sm_scale, void *o, float *lse, void *workspace,
-                              bsp_stream_t stream) {
+                              const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
+                              void *workspace, bsp_stream_t stream) {
     clear_error();
     int rc = check_plan(plan, BSP_MODE_DECODE, workspace);
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
-    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, workspace, stream);
+    if (num_pages < 0) return fail(BSP_ERR_INVALID_ARG, "num_pages must not be negative");
+    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
     if (rc != BSP_OK) return rc;
     return launch_reduce(plan, o, lse, workspace, stream);
 }
@@ -95,8 +96,10 @@ extern "C" int bsp_run_attention(const bsp_plan_info *plan, const void *q, const
     int rc = check_plan(plan, mode, workspace);
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
-    if (mode == BSP_MODE_DECODE)
-        return launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, workspace, stream);
+    if (mode == BSP_MODE_DECODE) {
+        if (num_pages < 0) return fail(BSP_ERR_INVALID_ARG, "num_pages must not be negative");
+        return launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
+    }
     if (num_pages < 1) return fail(BSP_ERR_INVALID_ARG, "num_pages must be positive");
     return launch_prefill(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
 }

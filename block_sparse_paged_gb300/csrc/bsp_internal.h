@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <string>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/bsp.h"
@@ -53,10 +54,16 @@ int last_code();
 
 inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
+// 3-D bf16 TMA map over a [rows][heads][dim] array (dim a multiple of 64):
+// boxes of 64 elements x box_heads x box_rows, 128-byte swizzle. BSP_OK or
+// BSP_ERR_* (unaligned base, encoder unavailable or rejecting the shape).
+int make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t dim, uint64_t heads, uint64_t rows, uint32_t box_heads,
+                   uint32_t box_rows);
+
 // Launchers (defined in the .cu files). They return BSP_OK or BSP_ERR_*.
 int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
-                  const void *v_pages, const int32_t *kv_indices, float sm_scale, void *o,
-                  float *lse, void *workspace, cudaStream_t stream);
+                  const void *v_pages, const int32_t *kv_indices, int64_t num_pages, float sm_scale,
+                  void *o, float *lse, void *workspace, cudaStream_t stream);
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages,
                    const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
                    float sm_scale, void *o, float *lse, void *workspace, cudaStream_t stream);

@@ -30,6 +30,8 @@
 // Reduction kernel: the reduction map's slots of each split output, merged in
 // ascending order with a common maximum (technical review eq 6), no atomics.
 #include <cfloat>
+#include <climits>
+#include <cstring>
 
 #include "bsp_internal.h"
 #include "device_common.cuh"
@@ -51,18 +53,27 @@ constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per
 constexpr int kStages = 5;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 
-template <int D>
+// kTma: K and V arrive by TMA tensor copies, one per page box, as 128-byte
+// swizzled [D / 64][64 rows][128 B] tiles; otherwise by 16-byte cp.async into
+// padded rows.
+template <int D, bool kTma>
 struct DecodeLayout {
-    static constexpr int kPitch = D * 2 + 16;              // padded row: ldmatrix phases hit 8 bank groups
-    static constexpr int kTileBytes = kTileK * kPitch;     // K (or V) part of a stage
+    static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 64-column slab
+    static constexpr int kSlab = kTma ? kTileK * 128 : 0;   // bytes per 64-column slab (TMA layout)
+    static constexpr int kTileBytes = kTma ? kTileK * D * 2 : kTileK * kPitch;  // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kScratchBytes = kConsumers * kMmaRows * D * 4;   // per-warp O rows for the item merge
     static constexpr int kStatBytes = kConsumers * kMmaRows * 2 * 4;      // per-warp (m, l)
     static constexpr int kBarOff = kRingBytes + kScratchBytes + kStatBytes;
     static constexpr int kNumBars = 2 * kStages + 2;        // full[S], empty[S], merge_in, merge_out
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
+    // byte offset of 16-byte chunk c (of D / 8) of ring row r inside a K or V tile
+    __device__ static __forceinline__ uint32_t chunk(int r, int c) {
+        if constexpr (kTma) return (uint32_t)((c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+        else return (uint32_t)(r * kPitch + c * 16);
+    }
 };
 
 struct DecodeParams {
@@ -74,6 +85,7 @@ struct DecodeParams {
     float *lse;
     float scale_log2;
     int H_qo, H_kv, g, page_size, tile_rows;
+    int box_rows;  // TMA gather: rows per tensor copy (divides page_size and 64)
 };
 
 // Status codes the decode kernel writes to the workspace status word.
@@ -92,10 +104,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const DecodeParams p) {
-    using LY = DecodeLayout<D>;
-    extern __shared__ __align__(128) uint8_t smem[];
+template <int D, bool kTma>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const DecodeParams p) {
+    using LY = DecodeLayout<D, kTma>;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = kTma ? smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023) : smem_raw;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
@@ -103,7 +118,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const Decode
     const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
-    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sbase = smem_u32(smem);  // 1024-byte aligned in the TMA layout
     const uint32_t full0 = sbase + LY::kBarOff, empty0 = full0 + kStages * 8;
     const uint32_t merge_in = empty0 + kStages * 8, merge_out = merge_in + 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + LY::kBarOff + LY::kNumBars * 8);
@@ -114,7 +129,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const Decode
     sm100::fence_proxy_async_smem();
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            sm100::mbar_init(full0 + 8 * s, 64);          // one no-increment arrival per producer lane
+            sm100::mbar_init(full0 + 8 * s, kTma ? 2 : 64);  // TMA: one per producer warp; else per lane
             sm100::mbar_init(empty0 + 8 * s, kConsumers);
         }
         sm100::mbar_init(merge_in, kConsumers);
@@ -122,9 +137,53 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const Decode
         *abort_flag = 0;
         sm100::fence_barrier_init();
     }
+    if (kTma && warp == kConsumers && lane == 0) {
+        sm100::prefetch_tmap(&tk);
+        sm100::prefetch_tmap(&tv);
+    }
     __syncthreads();
 
-    if (warp >= kConsumers) {
+    if (kTma && warp >= kConsumers) {
+        // ---------------- producers (TMA): warp 4 copies K, warp 5 V --------
+        // Lane i issues box i of the stage (box_rows rows of one page, D / 64
+        // tensor copies); lane 0 first posts the stage's byte count.
+        const bool is_v = warp == kConsumers + 1;
+        const CUtensorMap *map = is_v ? &tv : &tk;
+        const uint32_t part = is_v ? LY::kTileBytes : 0;
+        const int br = p.box_rows;
+        int k = 0;
+        for (int it = it0; it < it1 && !*abort_flag; ++it) {
+            const bsp_work_item w = items[it];
+            const int len = w.kv_end - w.kv_start;
+            const int nt = (len + kTileK - 1) / kTileK;
+            auto fetch = [&](int t) -> int {  // page id of this lane's box in stage t
+                const int r = t * kTileK + lane * br;
+                return (lane * br < kTileK && r < len) ? __ldg(p.kv_indices + w.page_base + (w.kv_start + r) / p.page_size)
+                                                       : 0;
+            };
+            int pg = nt > 0 ? fetch(0) : 0;
+            for (int t = 0; t < nt; ++t, ++k) {
+                const int n = min(kTileK, len - t * kTileK);
+                const int nbox = (n + br - 1) / br;
+                const int row0 = pg * p.page_size + (w.kv_start + t * kTileK + lane * br) % p.page_size;
+                if (t + 1 < nt) pg = fetch(t + 1);
+                const int s = k % kStages;
+                const bool ok = wait_or_abort(empty0 + 8 * s, ((k / kStages) & 1) ^ 1, abort_flag, status,
+                                              kStatusProducerWait);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                if (lane == 0) sm100::mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nbox * br * D * 2));
+                __syncwarp();
+                if (lane < nbox) {
+                    const uint32_t dst = sbase + s * LY::kStageBytes + part + (uint32_t)(lane * br * 128);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        sm100::tma_load_3d(dst + h * LY::kSlab, map, full0 + 8 * s, h * 64, w.kv_head, row0);
+                }
+            }
+        }
+        return;
+    }
+    if (!kTma && warp >= kConsumers) {
         // ---------------- producers: warp 4 copies K rows, warp 5 V rows ----
         // Each lane first turns the page ids of tokens `lane` and `lane + 32` of
         // the stage into byte offsets of their rows (one division each), then
@@ -220,17 +279,26 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const Decode
             if (valid > 0) {
                 const uint32_t kb = sbase + s * LY::kStageBytes;
                 const uint32_t vb = kb + LY::kTileBytes;
+                if (kTma && valid < 16) {
+                    // whole page boxes were copied: V rows of this warp past the chunk
+                    // end may hold anything; zero them so that P = 0 meets finite values
+                    for (int e = lane; e < (16 - valid) * (D / 8); e += 32) {
+                        const int row = warp * 16 + valid + e / (D / 8);
+                        *reinterpret_cast<uint4 *>(smem + (vb - sbase) + LY::chunk(row, e % (D / 8))) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
                 float sc[2][4];
 #pragma unroll
                 for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
                 {
                     const int mi = lane >> 3;
-                    const uint32_t rowaddr = kb + (uint32_t)(warp * 16 + (mi >> 1) * 8 + (lane & 7)) * LY::kPitch +
-                                             (uint32_t)(mi & 1) * 16;
+                    const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(rowaddr + kk * 32, b0, b1, b2, b3);
+                        ldmatrix_x4(kb + LY::chunk(row, 2 * kk + (mi & 1)), b0, b1, b2, b3);
                         mma_bf16_16816(sc[0], qa[kk], b0, b1);
                         mma_bf16_16816(sc[1], qa[kk], b2, b3);
                     }
@@ -283,17 +351,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_kernel(const Decode
                 pa[3] = pack_bf16(ps[1][2], ps[1][3]);
                 {
                     const int mi = lane >> 3;
-                    const uint32_t rowaddr = vb + (uint32_t)(warp * 16 + (mi & 1) * 8 + (lane & 7)) * LY::kPitch +
-                                             (uint32_t)(mi >> 1) * 16;
+                    const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
                     for (int nd = 0; nd < D / 16; ++nd) {
                         uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(rowaddr + nd * 32, b0, b1, b2, b3);
+                        ldmatrix_x4_trans(vb + LY::chunk(row, 2 * nd + (mi >> 1)), b0, b1, b2, b3);
                         mma_bf16_16816(acc[2 * nd], pa, b0, b1);
                         mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
                     }
                 }
             }
+            if (kTma) sm100::fence_proxy_async_smem();  // generic writes above before the next tensor copy
             __syncwarp();
             if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
         }
@@ -467,18 +535,19 @@ int num_sms_of_current_device(int *dev_out) {
     return sms[dev];
 }
 
-template <int D>
-int launch_decode_bf16(const DecodeParams &p, int grid, cudaStream_t stream) {
+template <int D, bool kTma>
+int launch_decode_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
+                       cudaStream_t stream) {
     static bool configured[64] = {false};
     int dev = 0;
     if (num_sms_of_current_device(&dev) < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecodeLayout<D>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecodeLayout<D, kTma>::kSmemBytes);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
         configured[dev] = true;
     }
-    decode_bf16_kernel<D><<<grid, kWsThreads, DecodeLayout<D>::kSmemBytes, stream>>>(p);
+    decode_bf16_kernel<D, kTma><<<grid, kWsThreads, DecodeLayout<D, kTma>::kSmemBytes, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
     return BSP_OK;
@@ -510,8 +579,8 @@ int decode_ctas_per_sm(int head_dim, int dtype) {
 }
 
 int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
-                  const int32_t *kv_indices, float sm_scale, void *o, float *lse, void *workspace,
-                  cudaStream_t stream) {
+                  const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
+                  void *workspace, cudaStream_t stream) {
     const bsp_problem &P = plan->problem;
     DecodeParams p;
     p.ws = static_cast<const uint8_t *>(workspace);
@@ -533,9 +602,28 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     const int grid = plan->capacity.num_ctas;
     if (P.dtype == BSP_DTYPE_BF16) {
         if (p.g > kMmaRows) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode needs num_qo_heads / num_kv_heads <= 16");
-        if (P.head_dim == 128) return launch_decode_bf16<128>(p, grid, stream);
-        if (P.head_dim == 64) return launch_decode_bf16<64>(p, grid, stream);
-        return fail(BSP_ERR_UNSUPPORTED, "bf16 decode supports head_dim 64 and 128");
+        if (P.head_dim != 128 && P.head_dim != 64) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode supports head_dim 64 and 128");
+        // Page rows are contiguous, so pages of 8 or more tokens (powers of two)
+        // are gathered by TMA, one tensor copy per page box; smaller pages by
+        // 16-byte cp.async. Without the pool size (num_pages 0) no map is made.
+        const int ps = P.page_size;
+        const bool tma = num_pages > 0 && ps >= 8 && (ps & (ps - 1)) == 0 &&
+                         num_pages * (int64_t)ps <= INT32_MAX;
+        CUtensorMap tk, tv;
+        std::memset(&tk, 0, sizeof(tk));
+        std::memset(&tv, 0, sizeof(tv));
+        if (tma) {
+            p.box_rows = ps < kTileK ? ps : kTileK;
+            const uint64_t rows = (uint64_t)num_pages * ps;
+            int rc = make_tmap_bf16(&tk, k_pages, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
+            if (rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
+            if (rc != BSP_OK) return rc;
+            return P.head_dim == 128 ? launch_decode_bf16<128, true>(tk, tv, p, grid, stream)
+                                     : launch_decode_bf16<64, true>(tk, tv, p, grid, stream);
+        }
+        p.box_rows = 0;
+        return P.head_dim == 128 ? launch_decode_bf16<128, false>(tk, tv, p, grid, stream)
+                                 : launch_decode_bf16<64, false>(tk, tv, p, grid, stream);
     }
     switch (P.head_dim) {
         case 32: return launch_decode_f32<32>(p, grid, stream);

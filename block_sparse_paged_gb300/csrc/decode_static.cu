@@ -87,7 +87,8 @@ extern "C" int bsp_decode_run_static(const bsp_plan_info *plan, const void *host
                             sizeof(bsp_merge_entry) * (size_t)plan->num_merges, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(dst + plan->off_status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("static plan copy: ") + cudaGetErrorString(e));
-    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, sm_scale, o, lse, ws, stream);
+    // no pool size here, so no tensor maps: pages are gathered with cp.async
+    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, 0, sm_scale, o, lse, ws, stream);
     if (rc != BSP_OK) return rc;
     return launch_reduce(plan, o, lse, ws, stream);
 }

@@ -529,43 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---- host: tensor maps -----------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// 3-D bf16 map (D innermost, then heads, then rows), 64-element x b1 x b2 box, 128-byte swizzle.
-int make_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows, uint32_t box_heads,
-             uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return fail(BSP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-    if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return fail(BSP_ERR_INVALID_ARG, "tensor base not 16-byte aligned");
-    cuuint64_t dims[3] = {(cuuint64_t)kD, heads, rows};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, heads * kD * 2};
-    cuuint32_t box[3] = {64, box_heads, box_rows};
-    cuuint32_t es[3] = {1, 1, 1};
-    std::memset(map, 0, sizeof(*map));
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(BSP_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
-    return BSP_OK;
-}
-
 }  // namespace
 
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
@@ -583,10 +546,10 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
 
     CUtensorMap tq, tk, tv;
     const int box_rows = P.page_size < kKvTile ? P.page_size : kKvTile;
-    int rc = make_map(&tq, q, P.num_qo_heads, (uint64_t)(plan->num_qo_tokens > 0 ? plan->num_qo_tokens : 1), g,
+    int rc = make_tmap_bf16(&tq, q, kD, P.num_qo_heads, (uint64_t)(plan->num_qo_tokens > 0 ? plan->num_qo_tokens : 1), g,
                       kRows / g);
-    if (rc == BSP_OK) rc = make_map(&tk, k_pages, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
-    if (rc == BSP_OK) rc = make_map(&tv, v_pages, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
+    if (rc == BSP_OK) rc = make_tmap_bf16(&tk, k_pages, kD, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
+    if (rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, kD, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
     if (rc != BSP_OK) return rc;
 
     PrefillParams p;

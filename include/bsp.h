@@ -211,6 +211,10 @@ int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity, int32_t b
  *   v_pages     device, [num_pages, page_size, H_kv, D]
  *   kv_indices  device, int32, the page ids (same array the plan's indptr
  *               indexes); may be NULL when no request has a page
+ *   num_pages   pages in the k_pages / v_pages pools: bounds the tensor maps
+ *               of the TMA page gather (pages of 8 or more tokens); 0 when
+ *               unknown, which gathers with cp.async instead; < 0 is
+ *               BSP_ERR_INVALID_ARG
  *   sm_scale    score scale (usually 1/sqrt(D))
  *   o           device, [n_tokens, H_qo, D], written
  *   lse         device, float [n_tokens, H_qo], written; may be NULL
@@ -218,8 +222,8 @@ int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity, int32_t b
  * Supported: bf16 with D in {64, 128} and g <= 16; fp32 with D <= 256.
  */
 int bsp_decode_run(const bsp_plan_info *plan, const void *q, const void *k_pages,
-                   const void *v_pages, const int32_t *kv_indices, float sm_scale,
-                   void *o, float *lse, void *workspace, bsp_stream_t stream);
+                   const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
+                   float sm_scale, void *o, float *lse, void *workspace, bsp_stream_t stream);
 
 /*
  * Prefill run: ragged queries, tiles of 256 packed rows (positions x g heads,
@@ -239,8 +243,8 @@ int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_page
  * (bsp_decode_run / bsp_prefill_run are exactly these two calls in order):
  *   bsp_run_attention       the attention kernel over the plan's work items
  *                           (final outputs for unsplit tiles, partial states in
- *                           the workspace for split ones); num_pages is used by
- *                           prefill and ignored by decode
+ *                           the workspace for split ones); num_pages as in
+ *                           bsp_decode_run / bsp_prefill_run
  *   bsp_run_merge_partials  the merge of partial states over the reduction map
  *                           (engineering walkthrough §VIII.4, the contraction
  *                           kernel); it always launches, with a fixed grid, and
@@ -284,7 +288,8 @@ int bsp_merge_state(const void *o_a, const float *lse_a, const void *o_b, const 
  *                 must not exceed BSP_STATIC_WORKSPACE_BYTES (else
  *                 BSP_ERR_CAPACITY: lower capacity.num_ctas or max_batch)
  *   host_staging  the staging buffer that bsp_plan wrote this plan into
- *   other arguments as in bsp_decode_run (device pointers, caller-owned).
+ *   other arguments as in bsp_decode_run (device pointers, caller-owned);
+ *   the pool size is not passed, so pages are gathered with cp.async.
  *
  * The array (BSP_STATIC_WORKSPACE_BYTES of device memory) exists once per
  * device in every process that loads the library and lives until the
