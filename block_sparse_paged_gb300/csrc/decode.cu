@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
     int *status = reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + p.off_status);
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
     const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
@@ -431,6 +432,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
     const float *qg = static_cast<const float *>(p.q);
     const float *kg = static_cast<const float *>(p.k);
     const float *vg = static_cast<const float *>(p.v);
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
     for (int it = queue[blockIdx.x]; it < queue[blockIdx.x + 1]; ++it) {
         const bsp_work_item w = items[it];
         for (int row = warp; row < p.g; row += kDecWarps) {
@@ -486,6 +488,10 @@ struct ReduceParams {
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
     constexpr int E = D / 32;
+    // Launched as a programmatic dependent of the attention kernel: it may be
+    // resident before that kernel ends, and waits here until its writes
+    // (partial states, the header) are complete and visible.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const DevHeader *hdr = reinterpret_cast<const DevHeader *>(p.ws + p.off_header);
     const bsp_merge_entry *merges = reinterpret_cast<const bsp_merge_entry *>(p.ws + p.off_merges);
     const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
@@ -565,8 +571,17 @@ template <int D, typename OutT>
 int launch_reduce_t(const ReduceParams &p, cudaStream_t stream) {
     const int sms = num_sms_of_current_device(nullptr);
     if (sms < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
-    reduce_kernel<D, OutT><<<2 * sms, 256, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sms);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap its launch with the kernel before it
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel<D, OutT>, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("reduce launch: ") + cudaGetErrorString(e));
     return BSP_OK;
 }

@@ -257,16 +257,14 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
     if (!merges.empty())
         std::memcpy(st + lay.off_merges, merges.data(), merges.size() * sizeof(bsp_merge_entry));
 
-    // ---- one H2D copy per used section, queued on the caller's stream -------
+    // ---- one H2D copy of the used prefix of the metadata, on the caller's stream
+    // (header, queue, the n items and, when there are merges, the unused item
+    // slots and the merges: the sections are contiguous in that order)
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaError_t err = cudaSuccess;
-    if (ws) err = cudaMemcpyAsync(ws, st, lay.off_items, cudaMemcpyHostToDevice, stream);
-    if (ws && err == cudaSuccess && n > 0)
-        err = cudaMemcpyAsync(ws + lay.off_items, st + lay.off_items, sizeof(bsp_work_item) * (size_t)n,
-                              cudaMemcpyHostToDevice, stream);
-    if (ws && err == cudaSuccess && !merges.empty())
-        err = cudaMemcpyAsync(ws + lay.off_merges, st + lay.off_merges, sizeof(bsp_merge_entry) * merges.size(),
-                              cudaMemcpyHostToDevice, stream);
+    const size_t used = merges.empty() ? lay.off_items + sizeof(bsp_work_item) * (size_t)n
+                                       : lay.off_merges + sizeof(bsp_merge_entry) * merges.size();
+    if (ws) err = cudaMemcpyAsync(ws, st, used, cudaMemcpyHostToDevice, stream);
     if (err != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("plan copy: ") + cudaGetErrorString(err));
 
     bsp_plan_info &o = *out;

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
     const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
