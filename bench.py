@@ -303,6 +303,16 @@ def run_ours(args, rank, world, local):
                 "traffic": profile_traffic("decode_bf16_batched", digest),
                 "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(attn_ms, 5)}
 
+    # host plan time alone (the planner's work plus queuing its one copy), after
+    # the timed region: reported separately from the run time
+    torch.cuda.synchronize()
+    n_plan = min(200, K)
+    tp = time.perf_counter()
+    for _ in range(n_plan):
+        pa.plan(batch.kv_indptr, batch.last_page_len)
+    plan_ms_host = (time.perf_counter() - tp) * 1e3 / n_plan
+    torch.cuda.synchronize()
+
     # end to end through the public API with host buffers
     e2e = run_e2e(bsp, batch, pa, K, W, dev, nbytes, world)
 
@@ -316,7 +326,8 @@ def run_ours(args, rank, world, local):
                    "num_ctas": num_ctas, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: 1.14 GB of KV per step vs 129 MB L2, no flush",
                    "step": "plan (host) + attention kernel + merge-of-partials kernel",
-                   "algorithmic_bytes_per_step": nbytes, "merge_ms": round(merge_ms, 5)},
+                   "algorithmic_bytes_per_step": nbytes, "merge_ms": round(merge_ms, 5),
+                   "plan_ms_host": round(plan_ms_host, 5)},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": 2 * K,
