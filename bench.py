@@ -453,8 +453,42 @@ def secondary(bsp, dev, args, pk):
         res["ragged_causal_prefill"] = {"unavailable": str(e)[:200]}
     del b
     torch.cuda.empty_cache()
+    res["vector_sparse_prefill"] = vector_sparse_prefill(bsp, dev, max(3, steps // 10), warm, pk)
     res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
     return res
+
+
+def vector_sparse_prefill(bsp, dev, steps, warm, pk):
+    """One 32768-token causal prefill with page size 1 (cp.async gather), once on
+    permuted slots and once contiguous: TFLOP/s of each and their ratio."""
+    import workloads
+    import dataclasses
+    perm, cont = workloads.vector_sparse_prefill_bf16()
+    n = int(cont.kv_indptr[-1])
+    # the same contiguous KV seen as 128-token pages: the dense-layout reference (TMA gather)
+    dense = dataclasses.replace(cont, name="vector_sparse_prefill_bf16_pages128", page_size=128,
+                                kv_indptr=np.array([0, n // 128], np.int32), kv_indices=np.arange(n // 128, dtype=np.int32),
+                                last_page_len=np.array([128], np.int32),
+                                k_pages=cont.k_pages.reshape(n // 128, 128, cont.num_kv_heads, cont.head_dim),
+                                v_pages=cont.v_pages.reshape(n // 128, 128, cont.num_kv_heads, cont.head_dim))
+    fl = prefill_flops(perm)
+    r = {}
+    for tag, b in (("permuted", perm), ("contiguous", cont), ("contiguous_pages128", dense)):
+        pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
+                                torch.bfloat16, max_batch=1, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+        attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
+        tf = fl / ((attn + merge) * 1e-3) / 1e12
+        r[tag] = {"TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                  "attn_ms": round(attn, 4), "merge_ms": round(merge, 4)}
+        del pa
+        torch.cuda.empty_cache()
+    r["permuted_over_contiguous"] = round(r["permuted"]["TFLOP/s"] / r["contiguous"]["TFLOP/s"], 4)
+    r["page1_over_pages128"] = round(r["permuted"]["TFLOP/s"] / r["contiguous_pages128"]["TFLOP/s"], 4)
+    r["flops"] = fl
+    r["workload"] = ("1 request, qo = kv = 32768, causal, page size 1 (slots permuted / contiguous; cp.async gather) "
+                     "and the same KV as 128-token pages (TMA gather), 32/8 heads, D 128, bf16")
+    r["pages_context"] = "FA3 template on H100: 532 (page 1) vs 627 (contiguous) TFLOP/s"
+    return r
 
 
 def shared_prefix_bytes(sp) -> int:

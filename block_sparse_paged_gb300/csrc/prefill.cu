@@ -91,10 +91,11 @@ struct PrefillParams {
     const uint8_t *ws;
     uint64_t off_queue, off_items, off_plse, off_po, off_status;
     const int32_t *kv_indices;
+    const char *k, *v;  // page pools (cp.async gather)
     void *o;
     float *lse;
     float scale_log2;
-    int H_qo, g, page_size, box_rows, causal, tile_rows;
+    int H_qo, H_kv, g, page_size, box_rows, causal, tile_rows;
 };
 
 struct Ctx {
@@ -145,6 +146,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// kTma: K and V tiles arrive by TMA tensor copies, one per page box (pages of
+// 8 or more tokens); otherwise by 16-byte cp.async copies written straight into
+// the same 128-byte-swizzled layout (pages of any size, e.g. 1).
+template <bool kTma>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -166,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool softmax_arrivals = i == kPFull0 || i == kPFull1 || i == kOFree0 || i == kOFree1;
-            mbar_init(bar(i), softmax_arrivals ? 128 : 1);
+            const bool kv_full = i == kKFull0 || i == kKFull1 || i == kVFull0 || i == kVFull1;
+            mbar_init(bar(i), softmax_arrivals ? 128 : (kv_full && !kTma) ? 32 : 1);  // cp.async: one per lane
         }
         *ctx.abort_flag = 0;
         fence_barrier_init();
@@ -211,35 +217,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sb + kOffQ + sub * kTile + h * kHalf, &tq, bar(kQFull), h * 64, w.kv_head * g,
                                     w.q_tok0 + sub * pos_per_sub);
             }
+            int pg_next[kKvTile / 32];  // cp.async gather: page ids of this lane's keys in the next tile
+            auto lookup = [&](int (&pg)[kKvTile / 32], int tt) {
+#pragma unroll
+                for (int i = 0; i < kKvTile / 32; ++i) {
+                    const int key = tt * kKvTile + lane + 32 * i;
+                    pg[i] = key < len ? __ldg(p.kv_indices + w.page_base + (w.kv_start + key) / p.page_size) : 0;
+                }
+            };
+            (void)lookup;
             for (int t = 0; t < nt; ++t, ++j) {
                 const int tok0 = w.kv_start + t * kKvTile;
                 const int valid = min(kKvTile, len - t * kKvTile);
-                const int nseg = (valid + p.box_rows - 1) / p.box_rows;
-                int page = 0;
-                if (lane < nseg) page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
-                const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
-                const uint32_t seg = (uint32_t)lane * p.box_rows * 128;
-                const uint32_t bytes = (uint32_t)nseg * p.box_rows * 128 * 2;
                 const int stage = j & 1, round = j >> 1;
-                if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kKFull0 + stage), bytes);
-                __syncwarp();
-                if (lane < nseg) {
-                    const uint32_t d = sb + kOffK + stage * kTile + seg;
-                    tma_load_3d(d, &tk, bar(kKFull0 + stage), 0, w.kv_head, row0);
-                    tma_load_3d(d + kHalf, &tk, bar(kKFull0 + stage), 64, w.kv_head, row0);
-                }
                 const int vst = j % kVStages, vrd = j / kVStages;
-                if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + vst), bytes);
-                __syncwarp();
-                if (lane < nseg) {
-                    const uint32_t d = sb + kOffV + vst * kTile + seg;
-                    tma_load_3d(d, &tv, bar(kVFull0 + vst), 0, w.kv_head, row0);
-                    tma_load_3d(d + kHalf, &tv, bar(kVFull0 + vst), 64, w.kv_head, row0);
+                if constexpr (kTma) {
+                    const int nseg = (valid + p.box_rows - 1) / p.box_rows;
+                    int page = 0;
+                    if (lane < nseg) page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
+                    const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
+                    const uint32_t seg = (uint32_t)lane * p.box_rows * 128;
+                    const uint32_t bytes = (uint32_t)nseg * p.box_rows * 128 * 2;
+                    if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
+                    if (lane == 0) mbar_arrive_expect_tx(bar(kKFull0 + stage), bytes);
+                    __syncwarp();
+                    if (lane < nseg) {
+                        const uint32_t d = sb + kOffK + stage * kTile + seg;
+                        tma_load_3d(d, &tk, bar(kKFull0 + stage), 0, w.kv_head, row0);
+                        tma_load_3d(d + kHalf, &tk, bar(kKFull0 + stage), 64, w.kv_head, row0);
+                    }
+                    if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
+                    if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + vst), bytes);
+                    __syncwarp();
+                    if (lane < nseg) {
+                        const uint32_t d = sb + kOffV + vst * kTile + seg;
+                        tma_load_3d(d, &tv, bar(kVFull0 + vst), 0, w.kv_head, row0);
+                        tma_load_3d(d + kHalf, &tv, bar(kVFull0 + vst), 64, w.kv_head, row0);
+                    }
+                } else {
+                    // Lane l looks up keys l + 32 i (page ids read one tile ahead); each
+                    // warp instruction then copies the sixteen 16-byte chunks of two keys
+                    // into their swizzled places. Keys past the chunk end are not copied
+                    // (their rows keep finite values).
+                    uint64_t off[kKvTile / 32];
+                    if (t == 0) lookup(pg_next, 0);
+#pragma unroll
+                    for (int i = 0; i < kKvTile / 32; ++i) {
+                        const int key = lane + 32 * i;
+                        const int tk_ = tok0 + key;
+                        off[i] = key < valid ? (((uint64_t)pg_next[i] * p.page_size + tk_ % p.page_size) * p.H_kv +
+                                                w.kv_head) * (kD * 2)
+                                             : 0;
+                    }
+                    if (t + 1 < nt) lookup(pg_next, t + 1);
+                    auto copy_tile = [&](const char *src, uint32_t dst, uint32_t full) {
+                        const int c = lane & 15;
+#pragma unroll
+                        for (int ii = 0; ii < kKvTile / 2; ++ii) {
+                            const int key = 2 * ii + (lane >> 4);  // key >> 5 == ii >> 4 for the whole warp
+                            const uint64_t o = __shfl_sync(0xffffffffu, off[ii >> 4], key & 31);
+                            if (key < valid)
+                                dev::cp_async_16(dst + (c >> 3) * kHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4),
+                                                 src + o + c * 16, 16);
+                        }
+                        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(full) : "memory");
+                    };
+                    if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
+                    copy_tile(p.k, sb + kOffK + stage * kTile, bar(kKFull0 + stage));
+                    if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
+                    copy_tile(p.v, sb + kOffV + vst * kTile, bar(kVFull0 + vst));
                 }
             }
         }
+        if constexpr (!kTma) asm volatile("cp.async.wait_all;\n" ::: "memory");  // nothing in flight at exit
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         // One thread issues everything: between MMA groups the tensor pipe
@@ -539,18 +589,21 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     const int g = plan->group;
     if (P.dtype != BSP_DTYPE_BF16) return fail(BSP_ERR_UNSUPPORTED, "prefill supports bf16 only");
     if (P.head_dim != kD) return fail(BSP_ERR_UNSUPPORTED, "prefill supports head_dim 128 only");
-    if (P.page_size < 8 || (P.page_size & (P.page_size - 1)) != 0)
-        return fail(BSP_ERR_UNSUPPORTED, "prefill needs page_size a power of two >= 8");
     if (plan->tile_rows != kSub * kRows || kRows % g != 0)
         return fail(BSP_ERR_UNSUPPORTED, "prefill needs 256-row tiles and 128 % g == 0");
-    if (num_pages * (int64_t)P.page_size > INT32_MAX) return fail(BSP_ERR_UNSUPPORTED, "KV pool beyond 2^31 rows");
+    // Pages of 8 or more tokens (powers of two) are gathered by TMA, one tensor
+    // copy per page box; other page sizes by 16-byte cp.async.
+    const int ps = P.page_size;
+    const bool tma = ps >= 8 && (ps & (ps - 1)) == 0 && num_pages * (int64_t)ps <= INT32_MAX;
 
     CUtensorMap tq, tk, tv;
-    const int box_rows = P.page_size < kKvTile ? P.page_size : kKvTile;
+    std::memset(&tk, 0, sizeof(tk));
+    std::memset(&tv, 0, sizeof(tv));
+    const int box_rows = tma ? (ps < kKvTile ? ps : kKvTile) : 1;
     int rc = make_tmap_bf16(&tq, q, kD, P.num_qo_heads, (uint64_t)(plan->num_qo_tokens > 0 ? plan->num_qo_tokens : 1), g,
                       kRows / g);
-    if (rc == BSP_OK) rc = make_tmap_bf16(&tk, k_pages, kD, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
-    if (rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, kD, P.num_kv_heads, (uint64_t)num_pages * P.page_size, 1, box_rows);
+    if (tma && rc == BSP_OK) rc = make_tmap_bf16(&tk, k_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
+    if (tma && rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
     if (rc != BSP_OK) return rc;
 
     PrefillParams p;
@@ -561,6 +614,9 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.off_po = plan->off_partial_o;
     p.off_status = plan->off_status;
     p.kv_indices = kv_indices;
+    p.k = static_cast<const char *>(k_pages);
+    p.v = static_cast<const char *>(v_pages);
+    p.H_kv = P.num_kv_heads;
     p.o = o;
     p.lse = lse;
     p.scale_log2 = sm_scale * dev::kLog2e;
@@ -571,15 +627,16 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.causal = P.causal;
     p.tile_rows = plan->tile_rows;
 
-    static bool configured[64] = {false};
+    static bool configured[2][64] = {{false}};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(BSP_ERR_CUDA, "no current CUDA device");
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    auto kern = tma ? prefill_kernel<true> : prefill_kernel<false>;
+    if (!configured[tma][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill smem attribute: ") + cudaGetErrorString(e));
-        configured[dev] = true;
+        configured[tma][dev] = true;
     }
-    prefill_kernel<<<plan->capacity.num_ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    kern<<<plan->capacity.num_ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
     return BSP_OK;

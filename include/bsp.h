@@ -232,7 +232,8 @@ int bsp_decode_run(const bsp_plan_info *plan, const void *q, const void *k_pages
  * overview ⑥, walkthrough §IV.2 and §V.4), then the merge of split outputs.
  *   num_pages   pages in the k_pages / v_pages pools (bounds of the gather)
  *   other arguments as in bsp_decode_run.
- * Supported: bf16, D = 128, 128 % g == 0, page_size a power of two >= 8.
+ * Supported: bf16, D = 128, 128 % g == 0; pages of 8 or more tokens (powers of
+ * two) are gathered with TMA tensor copies, other page sizes with cp.async.
  */
 int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_pages,
                     const void *v_pages, const int32_t *kv_indices, int64_t num_pages,

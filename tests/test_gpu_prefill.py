@@ -25,6 +25,9 @@ CASES = [
     (5, [64, 190, 3], [500, 190, 77], 16, 16, 128, False, 9),            # non-causal, g = 1
     (6, [128, 257], [128, 257], 64, 8, 16, True, 3),                     # g = 8
     (7, [1], [0], 32, 8, 16, True, 4),                                   # empty KV
+    (8, [65, 300, 17], [65, 300, 17], 32, 8, 1, True, 11),              # page size 1: cp.async gather
+    (9, [140, 33], [400, 33], 16, 4, 4, True, 6),                        # page size 4: cp.async gather
+    (10, [96, 250], [96, 700], 32, 8, 32, False, 5),                     # page 32 (two pages per box row set)
 ]
 
 
@@ -91,3 +94,28 @@ def test_shared_prefix_composable_full_size(bsp):
     tok, head = sample_rows(sp.full, 256, 22)
     O, L = oracle.attention_rows_of(sp.full, tok, head)
     compare(out, lse, O, L, "bf16", rows=(tok, head))
+
+
+def test_vector_sparse_prefill_small(bsp):
+    """Page size 1, one 1500-token causal prefill: permuted and contiguous slots
+    give bitwise equal outputs (same plan, only the gather differs) and match
+    the oracle everywhere."""
+    perm, cont = workloads.vector_sparse_prefill_bf16(1500, seed=61)
+    o1, l1, _ = run_batch(bsp, perm, mode="prefill", num_ctas=40)
+    o2, l2, _ = run_batch(bsp, cont, mode="prefill", num_ctas=40)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O, L = oracle_full(perm)
+    compare(o1, l1, O, L, "bf16")
+
+
+def test_vector_sparse_prefill_full_size(bsp):
+    """Page size 1, one 32768-token causal prefill (the long vector-sparse
+    prefill): sampled rows against the oracle, permuted == contiguous bitwise."""
+    perm, cont = workloads.vector_sparse_prefill_bf16()
+    o1, l1, pa = run_batch(bsp, perm, mode="prefill")
+    tok, head = sample_rows(perm, 192, 23)
+    O, L = oracle.attention_rows_of(perm, tok, head)
+    compare(o1, l1, O, L, "bf16", rows=(tok, head))
+    assert pa.check_device_error() == 0
+    o2, l2, _ = run_batch(bsp, cont, mode="prefill")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

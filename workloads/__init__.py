@@ -197,6 +197,33 @@ def vector_sparse_decode_bf16(batch: int = 32, kv_len: int = 4096, seed: int = 3
     return permuted, contiguous
 
 
+def vector_sparse_prefill_bf16(length: int = 32768, seed: int = 6, num_qo_heads: int = 32, num_kv_heads: int = 8):
+    """One causal prefill of `length` tokens (qo = kv), page size 1 with every
+    token slot of the pool permuted, 32 qo / 8 kv heads, head_dim 128, bf16.
+
+    Returns (permuted, contiguous): the same logical KV, once scattered and once
+    laid out in order (indices = arange)."""
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(length)
+    q = _normal(rng, (length, num_qo_heads, 128), "bf16")
+    k_log = _normal(rng, (length, 1, num_kv_heads, 128), "bf16")
+    v_log = _normal(rng, (length, 1, num_kv_heads, 128), "bf16")
+    k_perm = torch.empty_like(k_log)
+    v_perm = torch.empty_like(v_log)
+    pt = torch.from_numpy(perm)
+    k_perm[pt] = k_log
+    v_perm[pt] = v_log
+    ind = np.array([0, length], np.int32)
+    common = dict(dtype="bf16", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=128, page_size=1,
+                  causal=True, sm_scale=1.0 / math.sqrt(128), qo_indptr=ind.copy(), kv_indptr=ind.copy(),
+                  last_page_len=np.ones(1, np.int32), q=q)
+    permuted = PagedBatch(name="vector_sparse_prefill_bf16", kv_indices=perm.astype(np.int32),
+                          k_pages=k_perm, v_pages=v_perm, **common)
+    contiguous = PagedBatch(name="vector_sparse_prefill_bf16_contiguous",
+                            kv_indices=np.arange(length, dtype=np.int32), k_pages=k_log, v_pages=v_log, **common)
+    return permuted, contiguous
+
+
 def ragged_causal_prefill_bf16(batch: int = 16, seed: int = 4) -> PagedBatch:
     """batch 16, qo = kv ~ U{128..2048}, ragged Q, page 16 permuted, 32 qo / 8 kv
     heads, head_dim 128, bf16, causal (bottom-right)."""
