@@ -454,6 +454,17 @@ def secondary(bsp, dev, args, pk):
     del b
     torch.cuda.empty_cache()
     res["vector_sparse_prefill"] = vector_sparse_prefill(bsp, dev, max(3, steps // 10), warm, pk)
+    b = workloads.bsr_prefill_bf16()
+    pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
+                            torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+    attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
+    fl = prefill_flops(b)
+    res["bsr_prefill"] = {"TFLOP/s": round(fl / ((attn + merge) * 1e-3) / 1e12, 1), "attn_ms": round(attn, 4),
+                          "merge_ms": round(merge, 4), "flops": fl,
+                          "workload": "general BSR: 32 row blocks of 64 queries, 512 column blocks of 16 tokens, "
+                                      "25% block density, 32/8 heads, D 128, bf16, non-causal"}
+    del b, pa
+    torch.cuda.empty_cache()
     res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
     return res
 

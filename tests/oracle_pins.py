@@ -162,6 +162,27 @@ def pin_toy_bsr(orc):
         assert rows == pages, rows
 
 
+def pin_toy_bsr_attention(orc):
+    """Engineering walkthrough §V.1 with B_r = 4: the two query tiles (rows 0-3
+    and 4-7) share their tile's page list; each row's attention over the paged
+    pool must equal library softmax attention over exactly those pages."""
+    g = golden("toy_bsr.json")
+    D, br = 4, 4
+    rng = np.random.default_rng(13)
+    k = rng.standard_normal((6, 1, 1, D)).astype(np.float32)   # pages P0..P5, B_c = 1
+    v = rng.standard_normal((6, 1, 1, D)).astype(np.float32)
+    q = rng.standard_normal((2 * br, 1, D)).astype(np.float32)
+    qo_indptr = [0, br, 2 * br]
+    o, lse = orc.attention(q, k, v, qo_indptr, g["row_ptr"], g["col_indices"], [1, 1], 1, 1, 1, False, 0.5)
+    for tile, pages in enumerate(g["tile_pages"]):
+        rk = np.stack([k[pg, 0, 0] for pg in pages]).astype(np.float64)
+        rv = np.stack([v[pg, 0, 0] for pg in pages]).astype(np.float64)
+        for r in range(tile * br, (tile + 1) * br):
+            s = 0.5 * rk @ q[r, 0].astype(np.float64)
+            assert abs(lse[r, 0] - logsumexp(s)) < 1e-12
+            assert np.allclose(o[r, 0], softmax(s) @ rv, rtol=0, atol=1e-12)
+
+
 def pin_bsr_page_table(orc):
     """Overview ⑤: A -> pages 5,1,6; B -> 2; C -> 7,3 (indptr [0,3,4,6]).
 
@@ -293,6 +314,6 @@ def pin_poison_unread(orc):
 
 
 ALL_PINS = [pin_merge_worked_example, pin_merge_masses, pin_online_two_tiles, pin_one_key,
-            pin_page_mapping, pin_toy_bsr, pin_bsr_page_table, pin_dense_library,
+            pin_page_mapping, pin_toy_bsr, pin_toy_bsr_attention, pin_bsr_page_table, pin_dense_library,
             pin_permuted_equals_contiguous, pin_causal_prefix, pin_empty, pin_merge_algebra,
             pin_poison_unread]

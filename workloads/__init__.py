@@ -197,6 +197,40 @@ def vector_sparse_decode_bf16(batch: int = 32, kv_len: int = 4096, seed: int = 3
     return permuted, contiguous
 
 
+def bsr_prefill_bf16(seed: int = 7, n_row_blocks: int = 32, block_rows: int = 64, n_col_blocks: int = 512,
+                     block_cols: int = 16, density: float = 0.25, num_qo_heads: int = 32, num_kv_heads: int = 8,
+                     head_dim: int = 128):
+    """A general block-sparse (BSR) attention: n_row_blocks row blocks of
+    block_rows query rows; row block r attends to a seeded random subset (each
+    column block kept with probability `density`, at least one) of the
+    n_col_blocks column blocks of block_cols KV tokens, in a permuted order.
+    The column blocks are the pages of the pool (page size = block_cols) and may
+    be shared by several row blocks. Non-causal, bf16.
+
+    As a batch: request r = row block r, qo_indptr steps by block_rows, the page
+    list of request r is its column-block list (kv_indptr / kv_indices are the
+    BSR row_ptr / col_indices), every page full."""
+    rng = np.random.default_rng(seed)
+    lists = []
+    for _ in range(n_row_blocks):
+        keep = np.flatnonzero(rng.random(n_col_blocks) < density)
+        if keep.size == 0:
+            keep = rng.integers(0, n_col_blocks, size=1)
+        lists.append(rng.permutation(keep))
+    row_ptr = np.zeros(n_row_blocks + 1, np.int32)
+    row_ptr[1:] = np.cumsum([len(x) for x in lists])
+    col_indices = np.concatenate(lists).astype(np.int32)
+    n = n_row_blocks * block_rows
+    q = _normal(rng, (n, num_qo_heads, head_dim), "bf16")
+    k = _normal(rng, (n_col_blocks, block_cols, num_kv_heads, head_dim), "bf16")
+    v = _normal(rng, (n_col_blocks, block_cols, num_kv_heads, head_dim), "bf16")
+    return PagedBatch(name="bsr_prefill_bf16", dtype="bf16", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, page_size=block_cols, causal=False, sm_scale=1.0 / math.sqrt(head_dim),
+                      qo_indptr=(np.arange(n_row_blocks + 1) * block_rows).astype(np.int32), kv_indptr=row_ptr,
+                      kv_indices=col_indices, last_page_len=np.full(n_row_blocks, block_cols, np.int32),
+                      q=q, k_pages=k, v_pages=v)
+
+
 def vector_sparse_prefill_bf16(length: int = 32768, seed: int = 6, num_qo_heads: int = 32, num_kv_heads: int = 8):
     """One causal prefill of `length` tokens (qo = kv), page size 1 with every
     token slot of the pool permuted, 32 qo / 8 kv heads, head_dim 128, bf16.
