@@ -62,9 +62,9 @@ class PlanInfo(ctypes.Structure):
 WORK_ITEM_DTYPE = np.dtype([("b", "<i4"), ("tile", "<i4"), ("kv_head", "<i4"), ("kv_start", "<i4"),
                             ("kv_end", "<i4"), ("slot", "<i4"), ("q_tok0", "<i4"), ("n_pos", "<i4"),
                             ("qo_len", "<i4"), ("kv_len", "<i4"), ("page_base", "<i4"), ("pos0", "<i4"),
-                            ("reserved", "<i4", (4,))])
+                            ("merge", "<i4"), ("reserved", "<i4", (3,))])
 MERGE_ENTRY_DTYPE = np.dtype([("b", "<i4"), ("tile", "<i4"), ("kv_head", "<i4"), ("slot_begin", "<i4"),
-                              ("n_slots", "<i4"), ("q_tok0", "<i4"), ("n_pos", "<i4"), ("reserved", "<i4")])
+                              ("n_slots", "<i4"), ("q_tok0", "<i4"), ("n_pos", "<i4"), ("arrived", "<i4")])
 assert WORK_ITEM_DTYPE.itemsize == 64 and MERGE_ENTRY_DTYPE.itemsize == 32
 
 

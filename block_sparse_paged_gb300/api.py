@@ -177,9 +177,10 @@ class PagedAttention:
         return (out, lse) if return_lse else out
 
     def run_stages(self, q, k_pages, v_pages, kv_indices, sm_scale, out, lse, stream=None, events=None):
-        """The run as its two launches (attention kernel, merge of partials) on
-        `stream`; `events` = (e0, e1, e2) are recorded before, between and after
-        them when given. out and lse must be preallocated."""
+        """The run as its launches on `stream`: the attention kernel, then for
+        prefill the merge of partials (decode merges inside its kernel);
+        `events` = (e0, e1, e2) are recorded before, between and after them when
+        given. out and lse must be preallocated."""
         dev = self.device
         with torch.cuda.device(dev):
             st = stream if stream is not None else torch.cuda.current_stream()
@@ -196,7 +197,8 @@ class PagedAttention:
                                                ctypes.c_float(sm_scale), o_p, l_p, ws, s))
             if events:
                 events[1].record(st)
-            N.check(self.lib.bsp_run_merge_partials(ctypes.byref(self.info), o_p, l_p, ws, s))
+            if self.mode == N.BSP_MODE_PREFILL:  # decode merges split outputs inside its kernel
+                N.check(self.lib.bsp_run_merge_partials(ctypes.byref(self.info), o_p, l_p, ws, s))
             if events:
                 events[2].record(st)
         return out, lse

@@ -69,9 +69,9 @@ extern "C" int bsp_decode_run(const bsp_plan_info *plan, const void *q, const vo
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (num_pages < 0) return fail(BSP_ERR_INVALID_ARG, "num_pages must not be negative");
-    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
-    if (rc != BSP_OK) return rc;
-    return launch_reduce(plan, o, lse, workspace, stream);
+    // split outputs are merged inside the decode kernel (by the CTA that writes
+    // an output's last partial state): one launch
+    return launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
 }
 
 extern "C" int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,

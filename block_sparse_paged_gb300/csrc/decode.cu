@@ -66,7 +66,7 @@ struct DecodeLayout {
     static constexpr int kScratchBytes = kConsumers * kMmaRows * D * 4;   // per-warp O rows for the item merge
     static constexpr int kStatBytes = kConsumers * kMmaRows * 2 * 4;      // per-warp (m, l)
     static constexpr int kBarOff = kRingBytes + kScratchBytes + kStatBytes;
-    static constexpr int kNumBars = 2 * kStages + 2;        // full[S], empty[S], merge_in, merge_out
+    static constexpr int kNumBars = 2 * kStages + 3;        // full[S], empty[S], merge_in, merge_out, last
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
     // byte offset of 16-byte chunk c (of D / 8) of ring row r inside a K or V tile
@@ -86,7 +86,36 @@ struct DecodeParams {
     float scale_log2;
     int H_qo, H_kv, g, page_size, tile_rows;
     int box_rows;  // TMA gather: rows per tensor copy (divides page_size and 64)
+    uint64_t off_merges;
 };
+
+// Merge of one reduction-map entry by the threads t = 0..nthr-1 of the CTA
+// that wrote its last partial state: the left-to-right fold of its slots with
+// one common maximum (technical review §3.2 eq 6), final O and LSE written.
+// The partials were written by other CTAs: read through L2.
+template <int D, typename OutT>
+__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int t, int nthr) {
+    const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
+    const float *po = reinterpret_cast<const float *>(p.ws + p.off_po);
+    const int rows = e.n_pos * p.g;
+    for (int x = t; x < rows * D; x += nthr) {
+        const int r = x / D, d = x - r * D;
+        float M = -INFINITY;
+        for (int s = 0; s < e.n_slots; ++s) M = fmaxf(M, __ldcg(plse + (size_t)(e.slot_begin + s) * p.tile_rows + r));
+        float acc = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < e.n_slots; ++s) {
+                const size_t prow = (size_t)(e.slot_begin + s) * p.tile_rows + r;
+                const float wgt = exp2f((__ldcg(plse + prow) - M) * kLog2e);
+                L += wgt;
+                acc = fmaf(wgt, __ldcg(po + prow * D + d), acc);
+            }
+        }
+        const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
+        static_cast<OutT *>(p.o)[orow * D + d] = from_float<OutT>(M != -INFINITY ? acc / L : 0.f);
+        if (d == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
+    }
+}
 
 // Status codes the decode kernel writes to the workspace status word.
 constexpr int kStatusProducerWait = 0x101;
@@ -121,8 +150,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     const uint32_t sbase = smem_u32(smem);  // 1024-byte aligned in the TMA layout
     const uint32_t full0 = sbase + LY::kBarOff, empty0 = full0 + kStages * 8;
-    const uint32_t merge_in = empty0 + kStages * 8, merge_out = merge_in + 8;
+    const uint32_t merge_in = empty0 + kStages * 8, merge_out = merge_in + 8, last_bar = merge_out + 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + LY::kBarOff + LY::kNumBars * 8);
+    volatile int *last_flag = abort_flag + 1;  // "this CTA wrote an output's last partial"
 
     // Rows past a chunk's end are never copied: zero the ring once so that
     // they hold finite values (their probabilities are exactly 0).
@@ -135,6 +165,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         sm100::mbar_init(merge_in, kConsumers);
         sm100::mbar_init(merge_out, kConsumers);
+        sm100::mbar_init(last_bar, 1);
         *abort_flag = 0;
         sm100::fence_barrier_init();
     }
@@ -245,7 +276,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const int r0 = lane >> 2, r1 = r0 + 8;
     float *scratch = reinterpret_cast<float *>(smem + LY::kRingBytes);                       // [warp][16][D]
     float *stats = reinterpret_cast<float *>(smem + LY::kRingBytes + LY::kScratchBytes);   // [warp][16][m, l]
-    int k = 0, merges = 0;
+    int k = 0, merges = 0, lasts = 0;
+    bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
     for (int it = it0; it < it1; ++it) {
         const bsp_work_item w = items[it];
         const int len = w.kv_end - w.kv_start;
@@ -414,10 +446,29 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 if (d == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
             }
         }
+        if (w.slot >= 0) __threadfence();  // this thread's partial rows, before the arrival count below
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(merge_out);
         if (!__all_sync(0xffffffffu, wait_or_abort(merge_out, merges & 1, abort_flag, status, kStatusMergeWait))) return;
         ++merges;
+        if (w.slot >= 0) {
+            // Split output: count this partial in the reduction-map entry; the CTA
+            // whose partial completes the count merges all of them (nobody waits
+            // for another CTA, so no wait can depend on scheduling).
+            if (warp == 0 && lane == 0) {
+                const int prev = atomicAdd(&mmap[w.merge].arrived, 1);
+                *last_flag = prev == mmap[w.merge].n_slots - 1;
+                sm100::mbar_arrive(last_bar);
+            }
+            if (!__all_sync(0xffffffffu, wait_or_abort(last_bar, lasts & 1, abort_flag, status, kStatusMergeWait))) return;
+            ++lasts;
+            if (*last_flag) {
+                __threadfence();
+                const bsp_merge_entry e = mmap[w.merge];
+                merge_entry<D, __nv_bfloat16>(p, e, warp * 32 + lane, kConsumers * 32);
+                if (warp == 0 && lane == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
+            }
+        }
     }
 }
 
@@ -432,6 +483,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
     const float *qg = static_cast<const float *>(p.q);
     const float *kg = static_cast<const float *>(p.k);
     const float *vg = static_cast<const float *>(p.v);
+    bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
+    __shared__ int s_last;
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
     for (int it = queue[blockIdx.x]; it < queue[blockIdx.x + 1]; ++it) {
         const bsp_work_item w = items[it];
@@ -472,6 +525,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
                 for (int i = 0; i < E; ++i) po[lane + 32 * i] = acc[i] * inv;
                 if (lane == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
             }
+        }
+        if (w.slot >= 0) {
+            // split output: the CTA whose partial completes the count merges them all
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_last = atomicAdd(&mmap[w.merge].arrived, 1) == mmap[w.merge].n_slots - 1;
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const bsp_merge_entry e = mmap[w.merge];
+                merge_entry<D, float>(p, e, threadIdx.x, kDecThreads);
+                if (threadIdx.x == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
+            }
+            __syncthreads();
         }
     }
 }
@@ -604,6 +671,7 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     p.off_plse = plan->off_partial_lse;
     p.off_po = plan->off_partial_o;
     p.off_status = plan->off_status;
+    p.off_merges = plan->off_merges;
     p.q = q; p.k = k_pages; p.v = v_pages;
     p.kv_indices = kv_indices;
     p.o = o;

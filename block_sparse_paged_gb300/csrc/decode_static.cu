@@ -88,7 +88,6 @@ extern "C" int bsp_decode_run_static(const bsp_plan_info *plan, const void *host
     if (e == cudaSuccess) e = cudaMemsetAsync(dst + plan->off_status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("static plan copy: ") + cudaGetErrorString(e));
     // no pool size here, so no tensor maps: pages are gathered with cp.async
-    rc = launch_decode(plan, q, k_pages, v_pages, kv_indices, 0, sm_scale, o, lse, ws, stream);
-    if (rc != BSP_OK) return rc;
-    return launch_reduce(plan, o, lse, ws, stream);
+    // split outputs are merged inside the decode kernel
+    return launch_decode(plan, q, k_pages, v_pages, kv_indices, 0, sm_scale, o, lse, ws, stream);
 }

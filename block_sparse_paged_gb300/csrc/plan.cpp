@@ -80,7 +80,7 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
 namespace {
 
 struct Chunk {
-    int32_t b, tile, head, start, end, n_pos, slot;
+    int32_t b, tile, head, start, end, n_pos, slot, merge;
 };
 
 int64_t kv_len_of(const int32_t *kv_indptr, const int32_t *last_page_len, int page_size, int b) {
@@ -186,6 +186,7 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
                     ch.end = (int32_t)std::min<int64_t>((i + 1) * Lc, vis);
                     ch.n_pos = (int32_t)(p1 - p0);
                     ch.slot = n > 1 ? next_slot + (int32_t)i : -1;
+                    ch.merge = n > 1 ? (int32_t)merges.size() - 1 : -1;
                     chunks.push_back(ch);
                 }
                 if (n > 1) next_slot += (int32_t)n;
@@ -245,6 +246,7 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
             it.b = ch.b; it.tile = ch.tile; it.kv_head = ch.head;
             it.kv_start = ch.start; it.kv_end = ch.end; it.slot = ch.slot;
             it.pos0 = ch.tile * per_tile;
+            it.merge = ch.merge;
             it.q_tok0 = qo[ch.b] + it.pos0;
             it.n_pos = ch.n_pos;
             it.qo_len = qo[ch.b + 1] - qo[ch.b];

@@ -115,7 +115,8 @@ typedef struct bsp_work_item {
     int32_t kv_len;       /* KV tokens of request b                             */
     int32_t page_base;    /* kv_indptr[b]                                       */
     int32_t pos0;         /* tile's first query position within the request     */
-    int32_t reserved[4];
+    int32_t merge;        /* reduction-map entry of `slot`, or -1                */
+    int32_t reserved[3];
 } bsp_work_item;
 
 /* One entry of the reduction map (32 bytes): an output tile whose state is
@@ -124,7 +125,9 @@ typedef struct bsp_merge_entry {
     int32_t b, tile, kv_head;
     int32_t slot_begin, n_slots;
     int32_t q_tok0, n_pos;
-    int32_t reserved;
+    int32_t arrived;      /* device-side count of this entry's partial states
+                             written in the current run (0 when the plan is
+                             copied, and again after a run's merge)             */
 } bsp_merge_entry;
 
 /* Host-side description of a plan (filled by bsp_plan, passed to the runs). */
@@ -203,8 +206,11 @@ int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity, int32_t b
 
 /*
  * Decode run: split-KV attention with the g heads of a kv head fused into one
- * tile (engineering walkthrough §II.4; overview ⑦), then the merge of split
- * outputs over the reduction map (walkthrough §VIII.4-5).
+ * tile (engineering walkthrough §II.4; overview ⑦). Split outputs are merged
+ * over the reduction map (walkthrough §VIII.4-5) inside the same kernel: each
+ * CTA that writes a partial state counts it in the output's reduction-map
+ * entry, and the CTA whose partial completes the count folds them all (no CTA
+ * waits for another). One launch.
  *   plan        from bsp_plan with mode BSP_MODE_DECODE
  *   q           device, [n_tokens, H_qo, D]
  *   k_pages,
@@ -241,10 +247,12 @@ int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_page
 
 /*
  * The two stages of a run, for callers that time or schedule them apart
- * (bsp_decode_run / bsp_prefill_run are exactly these two calls in order):
+ * (bsp_prefill_run is exactly these two calls in order; bsp_decode_run is the
+ * first alone, and the second after it recomputes the same merged outputs):
  *   bsp_run_attention       the attention kernel over the plan's work items
  *                           (final outputs for unsplit tiles, partial states in
- *                           the workspace for split ones); num_pages as in
+ *                           the workspace for split ones, which decode also
+ *                           merges in the same kernel); num_pages as in
  *                           bsp_decode_run / bsp_prefill_run
  *   bsp_run_merge_partials  the merge of partial states over the reduction map
  *                           (engineering walkthrough §VIII.4, the contraction

@@ -43,3 +43,43 @@ def test_bsr_full_size(bsp):
     compare(out, lse, O, L, "bf16", rows=(tok, head))
     out2, lse2, _ = run_batch(bsp, b, mode="prefill")
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def variable_block_sparse(seed, row_sizes, col_sizes, density, hq, hk, D=128):
+    """Variable block sparse: row block i has row_sizes[i] queries, column block
+    j covers col_sizes[j] consecutive KV tokens; row block i attends to a seeded
+    random subset of column blocks. Expressed with page size 1: the page list of
+    row block i is the token slots of its column blocks."""
+    import math
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    starts = np.concatenate([[0], np.cumsum(col_sizes)])
+    n_kv = int(starts[-1])
+    lists = []
+    for _ in row_sizes:
+        keep = np.flatnonzero(rng.random(len(col_sizes)) < density)
+        if keep.size == 0:
+            keep = np.array([0])
+        lists.append(np.concatenate([np.arange(starts[j], starts[j + 1]) for j in keep]))
+    kv_indptr = np.zeros(len(row_sizes) + 1, np.int32)
+    kv_indptr[1:] = np.cumsum([len(x) for x in lists])
+    qo_indptr = np.zeros(len(row_sizes) + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(row_sizes)
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(int(qo_indptr[-1]), hq, D, generator=gen).to(torch.bfloat16)
+    k = torch.randn(n_kv, 1, hk, D, generator=gen).to(torch.bfloat16)
+    v = torch.randn(n_kv, 1, hk, D, generator=gen).to(torch.bfloat16)
+    return workloads.PagedBatch(name="variable_block_sparse", dtype="bf16", num_qo_heads=hq, num_kv_heads=hk,
+                                head_dim=D, page_size=1, causal=False, sm_scale=1.0 / math.sqrt(D),
+                                qo_indptr=qo_indptr, kv_indptr=kv_indptr, kv_indices=np.concatenate(lists).astype(np.int32),
+                                last_page_len=np.ones(len(row_sizes), np.int32), q=q, k_pages=k, v_pages=v)
+
+
+def test_variable_block_sparse(bsp):
+    """Row blocks of 7..90 queries, column blocks of 3..61 tokens: the page-size-1
+    gather covers any block sizes; against the oracle."""
+    b = variable_block_sparse(75, [7, 90, 33, 64, 12], [3, 61, 17, 40, 5, 29, 33, 8], 0.5, 16, 4)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=11)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0

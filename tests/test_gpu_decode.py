@@ -1,11 +1,14 @@
 """Decode path on the GPU through the C ABI, element by element against the
 oracle on the same seeded inputs."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
+from block_sparse_paged_gb300 import _native as N
 from gpu_helpers import (compare, lib, oracle_full, run_batch, sample_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -190,3 +193,30 @@ def test_run_rejects_bad_arguments(bsp):
         pa.run(q.float(), k, v, idx)         # wrong dtype
     with pytest.raises(ValueError):
         pa.run(q[:, :4], k, v, idx)          # wrong head count
+
+
+def test_fused_merge_repeated_runs(bsp):
+    """Split decode with the merge inside the kernel: three runs of one plan
+    (the arrival counters reset themselves) give identical results that match
+    the oracle, and an explicit merge-of-partials launch afterwards changes
+    nothing (it recomputes the same fold)."""
+    b = workloads.paged_batch(81, [1] * 9, [3000, 17, 900, 4100, 1, 2500, 64, 777, 1500], 32, 8, 128, 16, "bf16",
+                              extra_pages=3)
+    dev = to_dev(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=37, dev_tensors=dev)
+    assert pa.info.num_merges > 0
+    q, k, v, idx = dev
+    runs = [pa.run(q, k, v, idx, b.sm_scale) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o2, l2 in runs:
+        assert torch.equal(o2, out) and torch.equal(l2, lse)
+    O, L = oracle_full(b)
+    compare(out, lse, O, L, "bf16")
+    o3, l3 = out.clone(), lse.clone()
+    pa.run_stages(q, k, v, idx, b.sm_scale, o3, l3)
+    N.check(N.load().bsp_run_merge_partials(ctypes.byref(pa.info), ctypes.c_void_p(o3.data_ptr()),
+                                            ctypes.c_void_p(l3.data_ptr()), ctypes.c_void_p(pa.workspace.data_ptr()),
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    torch.cuda.synchronize()
+    assert torch.equal(o3, out) and torch.equal(l3, lse)
+    assert pa.check_device_error() == 0

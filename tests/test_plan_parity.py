@@ -56,6 +56,13 @@ def assert_same(info, queue, items, merges, ref, qo_indptr, kv_indptr):
         assert it["qo_len"] == qo_indptr[b + 1] - qo_indptr[b]
         assert it["page_base"] == kv_indptr[b]
         assert it["n_pos"] == min(int(it["qo_len"]), int(it["pos0"]) + per) - it["pos0"]
+        if it["slot"] < 0:
+            assert it["merge"] == -1
+        else:  # the reduction-map entry whose slot range holds the item's slot
+            m = merges[int(it["merge"])]
+            assert m["slot_begin"] <= it["slot"] < m["slot_begin"] + m["n_slots"]
+            assert (m["b"], m["tile"], m["kv_head"]) == (it["b"], it["tile"], it["kv_head"])
+    assert all(int(m["arrived"]) == 0 for m in merges)
 
 
 def test_lpt_worked_example(bsp):
