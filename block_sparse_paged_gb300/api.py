@@ -51,8 +51,9 @@ def default_num_ctas(mode: int, device: int | None = None) -> int:
 
 
 def make_problem(mode: int, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-                 causal: bool, dtype) -> N.Problem:
-    return N.Problem(mode, num_qo_heads, num_kv_heads, head_dim, page_size, int(bool(causal)), _DTYPES[dtype])
+                 causal: bool, dtype, window_left: int = -1, logits_soft_cap: float = 0.0) -> N.Problem:
+    return N.Problem(mode, num_qo_heads, num_kv_heads, head_dim, page_size, int(bool(causal)), _DTYPES[dtype],
+                     int(window_left), float(logits_soft_cap))
 
 
 def plan_host(problem: N.Problem, capacity: N.Capacity, kv_indptr, last_page_len, qo_indptr=None,
@@ -95,14 +96,16 @@ class PagedAttention:
 
     def __init__(self, mode: str, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  causal: bool = False, dtype=torch.bfloat16, max_batch: int = 256,
-                 max_qo_tokens: int | None = None, num_ctas: int | None = None, device=None):
+                 max_qo_tokens: int | None = None, num_ctas: int | None = None, device=None,
+                 window_left: int = -1, logits_soft_cap: float = 0.0):
         self.lib = N.load()
         if mode not in ("decode", "prefill"):
             raise ValueError("mode must be 'decode' or 'prefill'")
         self.mode = N.BSP_MODE_DECODE if mode == "decode" else N.BSP_MODE_PREFILL
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.dtype = dtype
-        self.problem = make_problem(self.mode, num_qo_heads, num_kv_heads, head_dim, page_size, causal, dtype)
+        self.problem = make_problem(self.mode, num_qo_heads, num_kv_heads, head_dim, page_size, causal, dtype,
+                                    window_left, logits_soft_cap)
         if num_ctas is None:
             num_ctas = default_num_ctas(self.mode, self.device.index)
         if max_qo_tokens is None:

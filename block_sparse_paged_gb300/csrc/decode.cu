@@ -87,6 +87,9 @@ struct DecodeParams {
     int H_qo, H_kv, g, page_size, tile_rows;
     int box_rows;  // TMA gather: rows per tensor copy (divides page_size and 64)
     uint64_t off_merges;
+    int window_left;         // > 0: keys j < pos + kv_len - qo_len - window_left are masked
+    int soft_cap_on;         // scores: tanh(s * cap_in) * cap_out instead of s * scale_log2
+    float cap_in, cap_out;   // sm_scale / c and c * log2(e)
 };
 
 // Merge of one reduction-map entry by the threads t = 0..nthr-1 of the CTA
@@ -309,6 +312,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
             if (!__all_sync(0xffffffffu, ok)) return;
             const int valid = min(kTileK, len - t * kTileK) - warp * 16;  // this warp's tokens
+            // sliding window: tokens of this warp before the window's edge (the chunk
+            // starts on a page boundary at or before it) are masked
+            const int lo_rel = p.window_left > 0
+                                   ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTileK + warp * 16)
+                                   : INT_MIN;
             if (valid > 0) {
                 const uint32_t kb = sbase + s * LY::kStageBytes;
                 const uint32_t vb = kb + LY::kTileBytes;
@@ -343,7 +351,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int tk = n * 8 + 2 * (lane & 3) + (c & 1);
-                        sc[n][c] = tk < valid ? sc[n][c] * p.scale_log2 : -INFINITY;
+                        const float x = p.soft_cap_on ? tanh_ex2(sc[n][c] * p.cap_in) * p.cap_out : sc[n][c] * p.scale_log2;
+                        sc[n][c] = (tk < valid && tk >= lo_rel) ? x : -INFINITY;
                     }
                     mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
                     mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
@@ -494,7 +503,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
 #pragma unroll
             for (int i = 0; i < E; ++i) { qr[i] = qg[qrow * D + lane + 32 * i]; acc[i] = 0.f; }
             float m = -INFINITY, l = 0.f;
-            for (int t = w.kv_start; t < w.kv_end; ++t) {
+            const int t_lo = p.window_left > 0 ? max(w.kv_start, w.pos0 + w.kv_len - w.qo_len - p.window_left)
+                                               : w.kv_start;  // sliding window's edge
+            for (int t = t_lo; t < w.kv_end; ++t) {
                 const int page = __ldg(p.kv_indices + w.page_base + t / p.page_size);
                 const size_t kr = ((size_t)page * p.page_size + t % p.page_size) * p.H_kv + w.kv_head;
                 float dot = 0.f;
@@ -502,7 +513,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
                 for (int i = 0; i < E; ++i) dot = fmaf(qr[i], kg[kr * D + lane + 32 * i], dot);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                const float x = dot * p.scale_log2;
+                const float x = p.soft_cap_on ? tanh_ex2(dot * p.cap_in) * p.cap_out : dot * p.scale_log2;
                 const float mn = fmaxf(m, x);
                 const float a = exp2f(m - mn), pe = exp2f(x - mn);
                 l = l * a + pe;
@@ -510,7 +521,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
                 for (int i = 0; i < E; ++i) acc[i] = fmaf(pe, vg[kr * D + lane + 32 * i], acc[i] * a);
                 m = mn;
             }
-            const bool empty = w.kv_end <= w.kv_start;
+            const bool empty = !(l > 0.f);  // no visible key (empty chunk, or all before the window)
             const float inv = empty ? 0.f : 1.f / l;
             const float lse_v = empty ? -INFINITY : (m + log2f(l)) * kLn2;
             if (w.slot < 0) {
@@ -677,6 +688,10 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     p.o = o;
     p.lse = lse;
     p.scale_log2 = sm_scale * kLog2e;
+    p.window_left = P.window_left;
+    p.soft_cap_on = P.logits_soft_cap > 0.f;
+    p.cap_in = p.soft_cap_on ? sm_scale / P.logits_soft_cap : 0.f;
+    p.cap_out = P.logits_soft_cap * kLog2e;
     p.H_qo = P.num_qo_heads;
     p.H_kv = P.num_kv_heads;
     p.g = plan->group;

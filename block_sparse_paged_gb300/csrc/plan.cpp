@@ -14,6 +14,8 @@
 #include <queue>
 #include <vector>
 
+#include <cmath>
+
 #include "bsp_internal.h"
 
 namespace bsp {
@@ -29,6 +31,8 @@ bool check_problem(const bsp_problem *p) {
     if (p->causal != 0 && p->causal != 1) return fail(BSP_ERR_INVALID_ARG, "causal must be 0 or 1"), false;
     if (p->dtype != BSP_DTYPE_BF16 && p->dtype != BSP_DTYPE_F32)
         return fail(BSP_ERR_INVALID_ARG, "dtype must be BSP_DTYPE_BF16 or BSP_DTYPE_F32"), false;
+    if (!(p->logits_soft_cap >= 0.f) || std::isinf(p->logits_soft_cap))
+        return fail(BSP_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0"), false;
     const int g = p->num_qo_heads / p->num_kv_heads;
     if (p->mode == BSP_MODE_PREFILL && (kPrefillTileRows / 2) % g != 0)
         return fail(BSP_ERR_UNSUPPORTED, "prefill needs 128 % (num_qo_heads / num_kv_heads) == 0"), false;
@@ -168,9 +172,17 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
         const int64_t ntiles = (qo_len * g + T - 1) / T;
         for (int64_t t = 0; t < ntiles; ++t) {
             const int64_t p0 = t * per_tile, p1 = std::min<int64_t>(qo_len, p0 + per_tile);
-            int64_t vis = kv_len;
+            int64_t vis = kv_len;  // keys [lo, vis) are visible to some row of the tile
             if (P.causal) vis = std::max<int64_t>(0, std::min<int64_t>(kv_len, (p1 - 1) + kv_len - qo_len + 1));
-            const int64_t n = vis == 0 ? 1 : (vis + Lc - 1) / Lc;
+            int64_t lo = 0;
+            if (P.window_left > 0) {
+                // the tile's first position sees the most keys from the left; rounded
+                // down to a page so that chunks never start inside a page
+                lo = std::max<int64_t>(0, p0 + kv_len - qo_len - P.window_left);
+                lo = lo / P.page_size * P.page_size;
+                if (lo >= vis) lo = vis = 0;  // nothing visible: one empty chunk
+            }
+            const int64_t n = vis == lo ? 1 : (vis - lo + Lc - 1) / Lc;
             for (int h = 0; h < H; ++h) {
                 if (n > 1) {
                     bsp_merge_entry m{};
@@ -182,8 +194,8 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
                 for (int64_t i = 0; i < n; ++i) {
                     Chunk ch;
                     ch.b = b; ch.tile = (int32_t)t; ch.head = h;
-                    ch.start = (int32_t)std::min<int64_t>(i * Lc, vis);
-                    ch.end = (int32_t)std::min<int64_t>((i + 1) * Lc, vis);
+                    ch.start = (int32_t)std::min<int64_t>(lo + i * Lc, vis);
+                    ch.end = (int32_t)std::min<int64_t>(lo + (i + 1) * Lc, vis);
                     ch.n_pos = (int32_t)(p1 - p0);
                     ch.slot = n > 1 ? next_slot + (int32_t)i : -1;
                     ch.merge = n > 1 ? (int32_t)merges.size() - 1 : -1;

@@ -96,6 +96,9 @@ struct PrefillParams {
     float *lse;
     float scale_log2;
     int H_qo, H_kv, g, page_size, box_rows, causal, tile_rows;
+    int window_left;         // > 0: key j is masked for a row at position i if j < i + kv_len - qo_len - window_left
+    int soft_cap_on;         // scores become tanh(s * cap_in); scale_log2 is then c * log2(e)
+    float cap_in;            // sm_scale / c
 };
 
 struct Ctx {
@@ -149,7 +152,9 @@ __device__ __forceinline__ float ex2(float x) {
 // kTma: K and V tiles arrive by TMA tensor copies, one per page box (pages of
 // 8 or more tokens); otherwise by 16-byte cp.async copies written straight into
 // the same 128-byte-swizzled layout (pages of any size, e.g. 1).
-template <bool kTma>
+// kVar: the sliding window and logits soft-cap variants are compiled in (the
+// default instantiation has neither, at no cost).
+template <bool kTma, bool kVar>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -402,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int len = w.kv_end - w.kv_start;
             const int nt = (len + kKvTile - 1) / kKvTile;
             const int pos = w.pos0 + rt / g;
+            const int lo = kVar && p.window_left > 0 ? pos + w.kv_len - w.qo_len - p.window_left : INT_MIN;  // window edge
             const int lim = p.causal ? pos + w.kv_len - w.qo_len : INT_MAX;  // key j allowed iff j <= lim
             asm volatile("" ::"r"(lim), "r"(len), "r"(w.kv_start));  // loaded before the S wait, not after
             float m = -INFINITY, l = 0.f;  // m: reference maximum (scaled, base 2)
@@ -420,10 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
                 }
                 tmem_wait_ld();
-                const bool full = valid == kKvTile && tok0 + kKvTile - 1 <= lim;
+                if (kVar && p.soft_cap_on) {  // technical review eq 8 (c * tanh(s / c), the factor c folded into scale_log2)
+#pragma unroll
+                    for (int c = 0; c < kKvTile; ++c) sv[c] = dev::tanh_ex2(sv[c] * p.cap_in);
+                }
+                const bool full = valid == kKvTile && tok0 + kKvTile - 1 <= lim && tok0 >= lo;
                 if (!full) {
 #pragma unroll
-                    for (int c = 0; c < kKvTile; ++c) sv[c] = (c < valid && tok0 + c <= lim) ? sv[c] : -INFINITY;
+                    for (int c = 0; c < kKvTile; ++c)
+                        sv[c] = (c < valid && tok0 + c <= lim && tok0 + c >= lo) ? sv[c] : -INFINITY;
                 }
                 // row maximum: 8 independent chains of 3-input maxima
                 float pm[8];
@@ -620,6 +631,10 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.o = o;
     p.lse = lse;
     p.scale_log2 = sm_scale * dev::kLog2e;
+    p.window_left = P.window_left;
+    p.soft_cap_on = P.logits_soft_cap > 0.f;
+    p.cap_in = p.soft_cap_on ? sm_scale / P.logits_soft_cap : 0.f;
+    if (p.soft_cap_on) p.scale_log2 = P.logits_soft_cap * dev::kLog2e;
     p.H_qo = P.num_qo_heads;
     p.g = g;
     p.page_size = P.page_size;
@@ -627,14 +642,17 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.causal = P.causal;
     p.tile_rows = plan->tile_rows;
 
-    static bool configured[2][64] = {{false}};
+    static bool configured[4][64] = {{false}};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(BSP_ERR_CUDA, "no current CUDA device");
-    auto kern = tma ? prefill_kernel<true> : prefill_kernel<false>;
-    if (!configured[tma][dev]) {
+    const bool var = P.window_left > 0 || P.logits_soft_cap > 0.f;
+    auto kern = tma ? (var ? prefill_kernel<true, true> : prefill_kernel<true, false>)
+                    : (var ? prefill_kernel<false, true> : prefill_kernel<false, false>);
+    const int which = (tma ? 2 : 0) + (var ? 1 : 0);
+    if (!configured[which][dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill smem attribute: ") + cudaGetErrorString(e));
-        configured[tma][dev] = true;
+        configured[which][dev] = true;
     }
     kern<<<plan->capacity.num_ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();

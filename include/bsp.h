@@ -88,9 +88,17 @@ typedef struct bsp_problem {
     int32_t num_qo_heads;  /* H_qo                                                 */
     int32_t num_kv_heads;  /* H_kv; H_qo % H_kv == 0, g = H_qo / H_kv             */
     int32_t head_dim;      /* D: 64 or 128 (prefill: 128)                         */
-    int32_t page_size;     /* B_c >= 1 (prefill: a power of two >= 8)             */
+    int32_t page_size;     /* B_c >= 1                                            */
     int32_t causal;        /* 0 or 1, bottom-right aligned                        */
     int32_t dtype;         /* BSP_DTYPE_BF16 or BSP_DTYPE_F32 (prefill: BF16)      */
+    /* Variants (FlashInfer 原理 overview, ⑧; FlashInfer: Making Attention Fit the
+     * Serving Workload, eq 8). Zero-initialised problems get neither.           */
+    int32_t window_left;   /* sliding window: query i sees key j only if
+                              j >= i + kv_len - qo_len - window_left; 0 or
+                              negative: no window (as -1)                         */
+    float logits_soft_cap; /* c > 0: scores s become c * tanh(s / c) (s already
+                              scaled by sm_scale) before masking and softmax;
+                              0: none                                            */
 } bsp_problem;
 
 /* Upper bounds fixed when the workspace is sized (technical review §6.4:

@@ -24,6 +24,12 @@
  *   - causal mask, bottom-right aligned: query i of a request with qo_len rows
  *     and kv_len keys sees key j iff j <= i + kv_len - qo_len (FlashInfer
  *     原理 overview, ⑧, the sink mask with the window term removed);
+ *   - sliding window (FlashInfer 原理 overview, ⑧, the sink variant's mask):
+ *     with window_left > 0, key j is also required to satisfy
+ *     j + qo_len + window_left >= kv_len + i;
+ *   - logits soft-cap (FlashInfer: Making Attention Fit the Serving Workload,
+ *     eq 8): with c = soft_cap > 0 each allowed score becomes c * tanh(s / c),
+ *     s being the scaled score, before the softmax;
  *   - stable merge with the empty-state rule (FlashInfer: Making Attention Fit
  *     the Serving Workload, §3.2 eq 6 and §3.3 Algorithm 1).
  *
@@ -84,6 +90,7 @@ static int32_t request_of_token(const int32_t *qo_indptr, int32_t batch, int64_t
  */
 int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
                           int32_t page_size, int32_t causal, double sm_scale,
+                          int32_t window_left, double soft_cap,
                           const int32_t *qo_indptr, const int32_t *kv_indptr,
                           const int32_t *kv_indices, const int32_t *last_page_len,
                           const float *q, const float *k_pages, const float *v_pages,
@@ -116,28 +123,34 @@ int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
             if (lim < n_vis) n_vis = lim;
             if (n_vis < 0) n_vis = 0;
         }
+        int64_t j0 = 0;                                          /* keys j >= j0 are allowed */
+        if (window_left > 0) {
+            j0 = i + kv_len - qo_len - window_left;              /* j + qo_len + window_left >= kv_len + i */
+            if (j0 < 0) j0 = 0;
+        }
         for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
-        if (n_vis == 0) { lse_out[s] = -INFINITY; continue; }
+        if (n_vis <= j0) { lse_out[s] = -INFINITY; continue; }
 
         const float *qv = q + (tok * H_qo + h) * (int64_t)D;
         double *sc = (double *)malloc(sizeof(double) * (size_t)n_vis);
         if (!sc) { bad = 1; continue; }
-        /* scores s_j = sm_scale * <q, k_j> */
-        for (int64_t j = 0; j < n_vis; ++j) {
+        /* scores s_j = sm_scale * <q, k_j> (then capped: c * tanh(s_j / c)) */
+        for (int64_t j = j0; j < n_vis; ++j) {
             int64_t row = oracle_physical_row(kv_indptr, kv_indices, page_size, b, j);
             const float *kv = k_pages + (row * H_kv + hk) * (int64_t)D;
             double acc = 0.0;
             for (int32_t d = 0; d < D; ++d) acc += (double)qv[d] * (double)kv[d];
             sc[j] = sm_scale * acc;
+            if (soft_cap > 0.0) sc[j] = soft_cap * tanh(sc[j] / soft_cap);
         }
         /* LSE = m + log sum exp(s_j - m) */
-        double m = sc[0];
-        for (int64_t j = 1; j < n_vis; ++j) if (sc[j] > m) m = sc[j];
+        double m = sc[j0];
+        for (int64_t j = j0 + 1; j < n_vis; ++j) if (sc[j] > m) m = sc[j];
         double z = 0.0;
-        for (int64_t j = 0; j < n_vis; ++j) z += exp(sc[j] - m);
+        for (int64_t j = j0; j < n_vis; ++j) z += exp(sc[j] - m);
         const double lse = m + log(z);
         /* O = sum_j exp(s_j - LSE) v_j */
-        for (int64_t j = 0; j < n_vis; ++j) {
+        for (int64_t j = j0; j < n_vis; ++j) {
             int64_t row = oracle_physical_row(kv_indptr, kv_indices, page_size, b, j);
             const float *vv = v_pages + (row * H_kv + hk) * (int64_t)D;
             const double p = exp(sc[j] - lse);

@@ -19,11 +19,17 @@ Attention Engine, §VIII.2 and §VIII.5):
 3. L = max(1, ceil(W / C)) (Algorithm 2 step 4 and the overview's worked
    example use the ceiling), then rounded up to a multiple of the page size so
    that no chunk splits a page.
-4. Each output tile's visible KV range [0, v) is cut into chunks of at most L
-   tokens (Algorithm 2 step 5). Non-causal: v = kv_len. Causal with
-   bottom-right alignment: v = min(kv_len, last_pos + kv_len - qo_len + 1)
-   clamped at 0, last_pos being the tile's largest query position. A tile
-   with v = 0 still gets one empty chunk so that its empty state is written.
+4. Each output tile's visible KV range [lo, v) is cut into chunks of at most
+   L tokens from lo on (Algorithm 2 step 5). Non-causal: v = kv_len. Causal
+   with bottom-right alignment: v = min(kv_len, last_pos + kv_len - qo_len + 1)
+   clamped at 0, last_pos being the tile's largest query position. lo = 0,
+   or with a sliding window of window_left > 0 (overview, ⑧: key j visible
+   from query i iff j + qo_len + window_left >= kv_len + i) the window's edge
+   for the tile's first position, first_pos + kv_len - qo_len - window_left,
+   clamped at 0 and rounded down to a page (this build's reading: chunks start
+   on page boundaries; the kernels mask the keys before the edge). A tile
+   with nothing visible (v <= lo) still gets one empty chunk (0, 0) so that its
+   empty state is written.
 5. Chunks are sorted by length, longest first, ties broken by the stable id
    (b, tile, kv_head, chunk_start) ascending (Algorithm 2 step 6).
 6. A min-heap of (cost, cta_id) starts at (0, c); each chunk goes to the popped
@@ -97,7 +103,8 @@ def visible_len(qo_len: int, kv_len: int, last_pos: int, causal: bool) -> int:
 
 
 def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
-         num_ctas: int, page_size: int, causal: bool, alpha: int = 2, beta: int = 1) -> Plan:
+         num_ctas: int, page_size: int, causal: bool, alpha: int = 2, beta: int = 1,
+         window_left: int = -1) -> Plan:
     if tile_rows % group != 0:
         raise ValueError("tile_rows must be a multiple of the group size")
     if num_ctas < 1 or page_size < 1:
@@ -105,14 +112,19 @@ def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
     B = len(qo_lens)
 
     # 1-2: output tiles and W
-    tiles = []  # (b, tile, kv_head, l_q, visible)
+    tiles = []  # (b, tile, kv_head, l_q, lo, visible)
     W = 0
     for b in range(B):
         for t in range(num_tiles(qo_lens[b], group, tile_rows)):
             p0, p1 = tile_positions(qo_lens[b], group, tile_rows, t)
             vis = visible_len(qo_lens[b], kv_lens[b], p1 - 1, causal)
+            lo = 0
+            if window_left > 0:
+                lo = max(0, p0 + kv_lens[b] - qo_lens[b] - window_left) // page_size * page_size
+                if lo >= vis:
+                    lo = vis = 0
             for h in range(num_kv_heads):
-                tiles.append((b, t, h, p1 - p0, vis))
+                tiles.append((b, t, h, p1 - p0, lo, vis))
                 W += kv_lens[b]
 
     # 3: chunk length
@@ -123,8 +135,8 @@ def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
     chunks = []  # (b, tile, kv_head, start, end, l_q, slot)
     outputs = []
     next_slot = 0
-    for (b, t, h, lq, vis) in tiles:
-        bounds = [(s, min(s + L, vis)) for s in range(0, vis, L)] or [(0, 0)]
+    for (b, t, h, lq, lo, vis) in tiles:
+        bounds = [(s, min(s + L, vis)) for s in range(lo, vis, L)] or [(0, 0)]
         if len(bounds) == 1:
             s, e = bounds[0]
             chunks.append((b, t, h, s, e, lq, -1))

@@ -30,7 +30,8 @@ def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=
     mode = mode or ("decode" if batch.is_decode else "prefill")
     pa = bsp.PagedAttention(mode, batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
                             batch.causal, TORCH[batch.dtype], max_batch=max_batch or batch.batch,
-                            max_qo_tokens=max_qo or int(batch.qo_indptr[-1]), num_ctas=num_ctas)
+                            max_qo_tokens=max_qo or int(batch.qo_indptr[-1]), num_ctas=num_ctas,
+                            window_left=batch.window_left, logits_soft_cap=batch.soft_cap)
     qo = None if mode == "decode" and batch.is_decode else batch.qo_indptr
     pa.plan(batch.kv_indptr, batch.last_page_len, qo_indptr=qo)
     q, k, v, idx = dev_tensors or to_dev(batch)
@@ -42,10 +43,13 @@ def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=
 def compare(out, lse, O_ref, L_ref, dtype, rows=None, rounding_aware=False):
     """Element-wise check of (out, lse) against the oracle's fp64 (O_ref, L_ref).
 
-    rounding_aware widens the O bound to max(tol, |O_ref| * 2^-8) for bf16: a
-    bf16 output of magnitude |x| carries up to |x| * 2^-8 of rounding alone
-    (8 significant bits), which exceeds 1e-2 once |x| > 2.56. Only used for
-    states that are not attention outputs of N(0, 1) values."""
+    bf16 outputs are compared after the GPU's cast: the bound on O is the
+    stated 1e-2 plus the cast's own rounding, at most |O_ref| * 2^-8 (half a
+    bf16 ulp; 8 significant bits). A row with two visible keys can reach
+    |O| ~ 2, where the cast alone is up to 0.0078.
+
+    rounding_aware instead bounds O by max(1e-2, |O_ref| * 2^-8) for bf16, for
+    states that are not attention outputs (merge inputs of any magnitude)."""
     o = out.float().cpu().numpy().astype(np.float64)
     l = lse.float().cpu().numpy().astype(np.float64)
     if rows is not None:
@@ -59,6 +63,10 @@ def compare(out, lse, O_ref, L_ref, dtype, rows=None, rounding_aware=False):
     if rounding_aware and dtype == "bf16":
         excess = np.abs(o - O_ref) - np.maximum(tol_o, np.abs(O_ref) * 2.0 ** -8)
         assert excess.max() <= 0, f"O error beyond the bf16 rounding bound by {excess.max()}"
+        tol_o = np.inf
+    elif dtype == "bf16" and o.size:
+        excess = np.abs(o - O_ref) - (tol_o + np.abs(O_ref) * 2.0 ** -8)
+        assert excess.max() <= 0, f"O error beyond 1e-2 + the bf16 cast bound by {excess.max()}"
         tol_o = np.inf
     err_o = np.abs(o - O_ref).max() if o.size else 0.0
     err_l = np.abs(l[fin] - L_ref[fin]).max() if fin.any() else 0.0

@@ -49,8 +49,10 @@ def dense_reference(batch: workloads.PagedBatch):
 
     The logical KV of request b is a plain slice of the flattened pool; query
     head h reads the h-th entry of the kv-head axis repeated g times; the
-    bottom-right causal mask is numpy's tril with offset kv_len - qo_len; the
-    softmax and log-sum-exp are scipy's."""
+    bottom-right causal mask is numpy's tril with offset kv_len - qo_len, the
+    sliding window numpy's triu with offset kv_len - qo_len - window_left, the
+    soft-cap numpy's tanh on the scaled scores; the softmax and log-sum-exp are
+    scipy's."""
     assert np.array_equal(batch.kv_indices, np.arange(len(batch.kv_indices)))
     kf = batch.k_pages.float().numpy().reshape(-1, batch.num_kv_heads, batch.head_dim)
     vf = batch.v_pages.float().numpy().reshape(-1, batch.num_kv_heads, batch.head_dim)
@@ -67,9 +69,14 @@ def dense_reference(batch: workloads.PagedBatch):
         V = np.repeat(vf[t0:t0 + kvl].astype(np.float64), g, axis=1)
         for h in range(batch.num_qo_heads):
             S = batch.sm_scale * qf[q0:q1, h] @ K[:, h].T               # [qo, kvl]
+            if batch.soft_cap > 0:
+                S = batch.soft_cap * np.tanh(S / batch.soft_cap)
+            allowed = np.ones((q1 - q0, kvl), bool)
             if batch.causal:
-                allowed = np.tril(np.ones((q1 - q0, kvl), bool), kvl - (q1 - q0))
-                S = np.where(allowed, S, -np.inf)
+                allowed &= np.tril(np.ones((q1 - q0, kvl), bool), kvl - (q1 - q0))
+            if batch.window_left > 0:
+                allowed &= np.triu(np.ones((q1 - q0, kvl), bool), kvl - (q1 - q0) - batch.window_left)
+            S = np.where(allowed, S, -np.inf)
             for i in range(q1 - q0):
                 if kvl == 0 or not np.isfinite(S[i]).any():
                     continue
@@ -82,7 +89,8 @@ def run_batch(orc, batch):
     return orc.attention(batch.q.float().numpy(), batch.k_pages.float().numpy(),
                          batch.v_pages.float().numpy(), batch.qo_indptr, batch.kv_indptr,
                          batch.kv_indices, batch.last_page_len, batch.num_qo_heads,
-                         batch.num_kv_heads, batch.page_size, batch.causal, batch.sm_scale)
+                         batch.num_kv_heads, batch.page_size, batch.causal, batch.sm_scale,
+                         window_left=batch.window_left, soft_cap=batch.soft_cap)
 
 
 # ---------------------------------------------------------------------------
@@ -230,6 +238,43 @@ def pin_dense_library(orc):
         assert np.allclose(O, Oe, rtol=0, atol=1e-12), i
 
 
+def pin_soft_cap_one_key(orc):
+    """Technical review eq 8 with one key: the state is that key's, O = v and
+    LSE = c * tanh(s / c), s the scaled score (closed form)."""
+    rng = np.random.default_rng(31)
+    D = 8
+    q = rng.standard_normal((1, 1, D)).astype(np.float32) * 3
+    k = rng.standard_normal((1, 1, 1, D)).astype(np.float32) * 3
+    v = rng.standard_normal((1, 1, 1, D)).astype(np.float32)
+    for c in (0.5, 2.0, 30.0):
+        o, lse = orc.attention(q, k, v, [0, 1], [0, 1], [0], [1], 1, 1, 1, False, 0.7, soft_cap=c)
+        s = 0.7 * float(np.dot(q[0, 0].astype(np.float64), k[0, 0, 0].astype(np.float64)))
+        assert abs(lse[0, 0] - c * np.tanh(s / c)) < 1e-12
+        assert np.allclose(o[0, 0], v[0, 0, 0], rtol=0, atol=1e-15)
+
+
+def pin_variants_library(orc):
+    """Sliding window and soft-cap on contiguous batches vs library routines on
+    the explicitly masked, explicitly capped dense scores."""
+    cases = [
+        dict(qo=[6, 9], kv=[6, 13], hq=4, hk=2, ps=4, causal=True, w=3, cap=0.0),
+        dict(qo=[1, 1, 1], kv=[9, 2, 17], hq=4, hk=4, ps=2, causal=True, w=5, cap=0.0),
+        dict(qo=[5, 3], kv=[11, 8], hq=6, hk=3, ps=3, causal=False, w=0, cap=1.5),
+        dict(qo=[7], kv=[12], hq=2, hk=1, ps=4, causal=True, w=4, cap=2.0),
+        dict(qo=[4], kv=[4], hq=2, hk=2, ps=1, causal=False, w=2, cap=0.0),
+    ]
+    for i, c in enumerate(cases):
+        batch = workloads.paged_batch(130 + i, c["qo"], c["kv"], c["hq"], c["hk"], 8, c["ps"], "f32",
+                                      causal=c["causal"], sm_scale=0.9, contiguous=True)
+        batch.window_left, batch.soft_cap = c["w"], c["cap"]
+        O, L = run_batch(orc, batch)
+        Oe, Le = dense_reference(batch)
+        assert np.array_equal(np.isinf(L), np.isinf(Le)), (i, L, Le)
+        fin = np.isfinite(Le)
+        assert np.allclose(L[fin], Le[fin], rtol=0, atol=1e-12), i
+        assert np.allclose(O, Oe, rtol=0, atol=1e-12), i
+
+
 def pin_permuted_equals_contiguous(orc):
     """Sparse and dense layouts of the same logical KV give identical fp64
     results (overview ⑥; walkthrough §V.4: the layouts differ only in the loader)."""
@@ -316,4 +361,4 @@ def pin_poison_unread(orc):
 ALL_PINS = [pin_merge_worked_example, pin_merge_masses, pin_online_two_tiles, pin_one_key,
             pin_page_mapping, pin_toy_bsr, pin_toy_bsr_attention, pin_bsr_page_table, pin_dense_library,
             pin_permuted_equals_contiguous, pin_causal_prefix, pin_empty, pin_merge_algebra,
-            pin_poison_unread]
+            pin_poison_unread, pin_soft_cap_one_key, pin_variants_library]

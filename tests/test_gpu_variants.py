@@ -1,0 +1,69 @@
+"""Attention variants (FlashInfer 原理 overview, ⑧; FlashInfer: Making Attention
+Fit the Serving Workload, eq 8): sliding window and logits soft-cap, on the
+decode and prefill paths, against the oracle on the same seeded inputs."""
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import compare, lib, oracle_full, run_batch, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    return lib()
+
+
+def with_variant(b, window_left=-1, soft_cap=0.0):
+    b.window_left, b.soft_cap = window_left, soft_cap
+    return b
+
+
+DECODE = [
+    # (seed, kv lens, H_qo, H_kv, D, page, dtype, window, cap, num_ctas)
+    (91, [3000, 17, 900, 4100, 1, 250], 32, 8, 128, 16, "bf16", 700, 0.0, 29),     # window, splits
+    (92, [3000, 17, 900, 4100, 1, 250], 32, 8, 128, 16, "bf16", -1, 1.5, 29),      # soft-cap
+    (93, [2000, 64, 1500], 64, 8, 128, 1, "bf16", 333, 2.0, 11),                   # both, page size 1
+    (94, [700, 5, 1200], 16, 4, 64, 4, "f32", 100, 3.0, 9),                        # fp32 path
+]
+
+
+@pytest.mark.parametrize("case", DECODE, ids=[f"decode{c[0]}" for c in DECODE])
+def test_decode_variants(bsp, case):
+    seed, kv, hq, hk, D, ps, dt, w, cap, C = case
+    b = with_variant(workloads.paged_batch(seed, [1] * len(kv), kv, hq, hk, D, ps, dt, extra_pages=2), w, cap)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=C)
+    compare(out, lse, O, L, dt)
+    assert pa.check_device_error() == 0
+
+
+PREFILL = [
+    # (seed, qo lens, kv lens, H_qo, H_kv, page, causal, window, cap, num_ctas)
+    (95, [300, 65, 1000], [300, 65, 1000], 32, 8, 16, True, 150, 0.0, 13),
+    (96, [300, 65, 1000], [300, 65, 1000], 32, 8, 16, True, -1, 1.5, 13),
+    (97, [200, 90], [700, 90], 16, 4, 1, True, 77, 2.5, 7),      # page size 1, qo < kv, both
+    (98, [128, 300], [128, 500], 32, 8, 32, False, 100, 0.0, 9),  # non-causal window
+]
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=[f"prefill{c[0]}" for c in PREFILL])
+def test_prefill_variants(bsp, case):
+    seed, qo, kv, hq, hk, ps, causal, w, cap, C = case
+    b = with_variant(workloads.paged_batch(seed, qo, kv, hq, hk, 128, ps, "bf16", causal=causal, extra_pages=2),
+                     w, cap)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=C)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_prefill_window_full_size(bsp):
+    """The ragged causal prefill workload with a 512-token window and a soft-cap
+    of 30: sampled rows against the oracle."""
+    b = with_variant(workloads.ragged_causal_prefill_bf16(), 512, 30.0)
+    out, lse, pa = run_batch(bsp, b, mode="prefill")
+    tok, head = sample_rows(b, 256, 25)
+    O, L = oracle.attention_rows_of(b, tok, head)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))

@@ -34,6 +34,8 @@ MUTATIONS = [
     ("merge_lse_missing_max", "lse_out[s] = m + log(a + bb);", "lse_out[s] = log(a + bb);"),
     ("merge_empty_passes_wrong_side", "for (int32_t d = 0; d < D; ++d) o[d] = oa[d];\n            lse_out[s] = la;",
      "for (int32_t d = 0; d < D; ++d) o[d] = ob[d];\n            lse_out[s] = lb;"),
+    ("soft_cap_scale_dropped", "sc[j] = soft_cap * tanh(sc[j] / soft_cap);", "sc[j] = tanh(sc[j]);"),
+    ("window_off_by_one", "j0 = i + kv_len - qo_len - window_left;", "j0 = i + kv_len - qo_len - window_left + 1;"),
     ("merge_naive_average", "o[d] = (a * oa[d] + bb * ob[d]) / (a + bb);", "o[d] = 0.5 * (oa[d] + ob[d]);"),
 ]
 

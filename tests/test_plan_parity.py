@@ -16,7 +16,7 @@ def bsp():
 
 
 def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alpha=2, beta=1, D=128,
-             max_batch=None, max_qo=None):
+             max_batch=None, max_qo=None, window_left=-1):
     qo_lens = np.asarray(qo_lens, np.int64)
     kv_lens = np.asarray(kv_lens, np.int64)
     B = len(kv_lens)
@@ -27,13 +27,15 @@ def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alph
     qo_indptr = np.zeros(B + 1, np.int32)
     qo_indptr[1:] = np.cumsum(qo_lens)
     g = H_qo // H_kv
-    prob = bsp.make_problem(mode, H_qo, H_kv, D, page_size, causal, __import__("torch").bfloat16)
+    prob = bsp.make_problem(mode, H_qo, H_kv, D, page_size, causal, __import__("torch").bfloat16,
+                            window_left=window_left)
     cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]))
     info, queue, items, merges = bsp.plan_host(prob, cap, kv_indptr, last,
                                                None if mode == bsp.BSP_MODE_DECODE and np.all(qo_lens == 1) else qo_indptr,
                                                alpha, beta)
     tile = g if mode == bsp.BSP_MODE_DECODE else 256
-    ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta)
+    ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta,
+                     window_left=window_left)
     return info, queue, items, merges, ref, qo_indptr, kv_indptr
 
 
@@ -128,3 +130,38 @@ def test_partials_within_eq13_bound(bsp):
         info, *_ = run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(B, int), kv, 16, 32, 8, False, C)
         assert info.num_partials <= 2 * C <= info.cap_partials
         assert info.num_items <= info.cap_items and info.num_merges <= info.cap_merges
+
+
+@pytest.mark.parametrize("case", [
+    # (mode, qo lens, kv lens, page, H_qo, H_kv, causal, C, window_left)
+    ("decode", [1] * 6, [900, 30, 2000, 1, 513, 64], 16, 32, 8, False, 13, 100),
+    ("decode", [1] * 4, [40, 300, 7, 1000], 1, 8, 8, False, 5, 33),
+    ("prefill", [300, 65, 1200], [300, 65, 1500], 16, 32, 8, True, 11, 200),
+    ("prefill", [700, 90], [700, 400], 8, 16, 4, True, 7, 64),
+    ("prefill", [128, 40], [500, 40], 4, 8, 8, False, 9, 17),
+])
+def test_window_plan_parity_and_coverage(bsp, case):
+    """Sliding window: the C planner equals the oracle planner bit for bit, and
+    the chunks of every output tile cover each of its rows' visible keys
+    (j <= i + kv_len - qo_len when causal, j >= i + kv_len - qo_len - w) once."""
+    mode_s, qo, kv, ps, hq, hk, causal, C, w = case
+    mode = bsp.BSP_MODE_DECODE if mode_s == "decode" else bsp.BSP_MODE_PREFILL
+    info, queue, items, merges, ref, qo_indptr, kv_indptr = run_both(bsp, mode, qo, kv, ps, hq, hk, causal, C,
+                                                                    window_left=w)
+    assert_same(info, queue, items, merges, ref, qo_indptr, kv_indptr)
+    per = info.tile_rows // info.group
+    covered = {}
+    for it in items:
+        key = (int(it["b"]), int(it["tile"]), int(it["kv_head"]))
+        covered.setdefault(key, []).append((int(it["kv_start"]), int(it["kv_end"])))
+    for (b, t, h), ranges in covered.items():
+        ranges.sort()
+        for (s0, e0), (s1, e1) in zip(ranges, ranges[1:]):
+            assert e0 == s1  # contiguous, no overlap
+        lo, hi = ranges[0][0], ranges[-1][1]
+        for p in range(t * per, min(qo[b], (t + 1) * per)):
+            vis_hi = min(kv[b], p + kv[b] - qo[b] + 1) if causal else kv[b]
+            vis_lo = max(0, p + kv[b] - qo[b] - w)
+            if vis_hi > vis_lo:
+                assert lo <= vis_lo and vis_hi <= hi, (b, t, p, lo, hi, vis_lo, vis_hi)
+                assert lo % ps == 0

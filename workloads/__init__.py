@@ -48,6 +48,8 @@ class PagedBatch:
     k_pages: torch.Tensor      # [num_pages, page_size, H_kv, D]
     v_pages: torch.Tensor
     meta: dict = field(default_factory=dict)
+    window_left: int = -1    # sliding window (> 0) or none
+    soft_cap: float = 0.0    # logits soft-cap c (> 0) or none
 
     @property
     def batch(self) -> int:
