@@ -87,36 +87,54 @@ struct DecodeParams {
     int H_qo, H_kv, g, page_size, tile_rows;
     int box_rows;  // TMA gather: rows per tensor copy (divides page_size and 64)
     uint64_t off_merges;
+    int queues_per_cta, num_queues;  // CTA b runs plan queues [b * qpc, min((b + 1) * qpc, C))
     int window_left;         // > 0: keys j < pos + kv_len - qo_len - window_left are masked
     int soft_cap_on;         // scores: tanh(s * cap_in) * cap_out instead of s * scale_log2
     float cap_in, cap_out;   // sm_scale / c and c * log2(e)
 };
 
-// Merge of one reduction-map entry by the threads t = 0..nthr-1 of the CTA
-// that wrote its last partial state: the left-to-right fold of its slots with
-// one common maximum (technical review §3.2 eq 6), final O and LSE written.
-// The partials were written by other CTAs: read through L2.
+// Merge of one reduction-map entry by warps w = 0..nwarps-1 of the CTA that
+// wrote its last partial state: the fold of its slots with one common maximum
+// (technical review §3.2 eq 6), final O and LSE written. One warp per output
+// row: lanes read the slots' LSEs side by side (32 at a time), the maximum and
+// the weights come by shuffle, and each lane folds its own D / 32 columns with
+// independent loads. The partials were written by other CTAs: read through L2.
 template <int D, typename OutT>
-__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int t, int nthr) {
+__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int w, int nwarps,
+                                            int lane) {
+    constexpr int E = D / 32;
     const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
     const float *po = reinterpret_cast<const float *>(p.ws + p.off_po);
     const int rows = e.n_pos * p.g;
-    for (int x = t; x < rows * D; x += nthr) {
-        const int r = x / D, d = x - r * D;
+    for (int r = w; r < rows; r += nwarps) {
         float M = -INFINITY;
-        for (int s = 0; s < e.n_slots; ++s) M = fmaxf(M, __ldcg(plse + (size_t)(e.slot_begin + s) * p.tile_rows + r));
-        float acc = 0.f, L = 0.f;
+        for (int s0 = 0; s0 < e.n_slots; s0 += 32)
+            if (s0 + lane < e.n_slots) M = fmaxf(M, __ldcg(plse + (size_t)(e.slot_begin + s0 + lane) * p.tile_rows + r));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float acc[E], L = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[i] = 0.f;
         if (M != -INFINITY) {
-            for (int s = 0; s < e.n_slots; ++s) {
-                const size_t prow = (size_t)(e.slot_begin + s) * p.tile_rows + r;
-                const float wgt = exp2f((__ldcg(plse + prow) - M) * kLog2e);
-                L += wgt;
-                acc = fmaf(wgt, __ldcg(po + prow * D + d), acc);
+            for (int s0 = 0; s0 < e.n_slots; s0 += 32) {
+                const int ns = min(32, e.n_slots - s0);
+                const size_t prow0 = (size_t)(e.slot_begin + s0) * p.tile_rows + r;
+                const float my_w = lane < ns ? exp2f((__ldcg(plse + prow0 + (size_t)lane * p.tile_rows) - M) * kLog2e) : 0.f;
+                for (int s = 0; s < ns; ++s) {
+                    const float wgt = __shfl_sync(0xffffffffu, my_w, s);
+                    const float *src = po + (prow0 + (size_t)s * p.tile_rows) * D + lane * E;
+                    L += wgt;
+#pragma unroll
+                    for (int i = 0; i < E; ++i) acc[i] = fmaf(wgt, __ldcg(src + i), acc[i]);
+                }
             }
         }
+        const float inv = M != -INFINITY ? 1.f / L : 0.f;
         const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
-        static_cast<OutT *>(p.o)[orow * D + d] = from_float<OutT>(M != -INFINITY ? acc / L : 0.f);
-        if (d == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
+        OutT *dst = static_cast<OutT *>(p.o) + orow * D + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) dst[i] = from_float<OutT>(acc[i] * inv);
+        if (lane == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
     }
 }
 
@@ -148,7 +166,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
     int *status = reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + p.off_status);
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
-    const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
+    const int qb = blockIdx.x * p.queues_per_cta;
+    const int it0 = queue[qb], it1 = queue[min(qb + p.queues_per_cta, p.num_queues)];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
     const uint32_t sbase = smem_u32(smem);  // 1024-byte aligned in the TMA layout
@@ -474,7 +493,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (*last_flag) {
                 __threadfence();
                 const bsp_merge_entry e = mmap[w.merge];
-                merge_entry<D, __nv_bfloat16>(p, e, warp * 32 + lane, kConsumers * 32);
+                merge_entry<D, __nv_bfloat16>(p, e, warp, kConsumers, lane);
                 if (warp == 0 && lane == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
             }
         }
@@ -495,7 +514,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
     bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
     __shared__ int s_last;
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
-    for (int it = queue[blockIdx.x]; it < queue[blockIdx.x + 1]; ++it) {
+    const int qb = blockIdx.x * p.queues_per_cta;
+    for (int it = queue[qb]; it < queue[min(qb + p.queues_per_cta, p.num_queues)]; ++it) {
         const bsp_work_item w = items[it];
         for (int row = warp; row < p.g; row += kDecWarps) {
             const size_t qrow = (size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * p.g + row;
@@ -546,7 +566,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
             if (s_last) {
                 __threadfence();
                 const bsp_merge_entry e = mmap[w.merge];
-                merge_entry<D, float>(p, e, threadIdx.x, kDecThreads);
+                merge_entry<D, float>(p, e, threadIdx.x >> 5, kDecWarps, threadIdx.x & 31);
                 if (threadIdx.x == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
             }
             __syncthreads();
@@ -697,7 +717,14 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     p.g = plan->group;
     p.page_size = P.page_size;
     p.tile_rows = plan->tile_rows;
-    const int grid = plan->capacity.num_ctas;
+    // A plan may have more queues than CTAs fit on the GPU at once: each CTA then
+    // runs several consecutive queues (one wave; the planner balanced every queue).
+    const int sms = num_sms_of_current_device(nullptr);
+    if (sms < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    const int resident = sms * decode_ctas_per_sm(P.head_dim, P.dtype);
+    p.num_queues = plan->capacity.num_ctas;
+    p.queues_per_cta = (p.num_queues + resident - 1) / resident;
+    const int grid = (p.num_queues + p.queues_per_cta - 1) / p.queues_per_cta;
     if (P.dtype == BSP_DTYPE_BF16) {
         if (p.g > kMmaRows) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode needs num_qo_heads / num_kv_heads <= 16");
         if (P.head_dim != 128 && P.head_dim != 64) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode supports head_dim 64 and 128");

@@ -96,6 +96,7 @@ struct PrefillParams {
     float *lse;
     float scale_log2;
     int H_qo, H_kv, g, page_size, box_rows, causal, tile_rows;
+    int queues_per_cta, num_queues;  // CTA b runs plan queues [b * qpc, min((b + 1) * qpc, C))
     int window_left;         // > 0: key j is masked for a row at position i if j < i + kv_len - qo_len - window_left
     int soft_cap_on;         // scores become tanh(s * cap_in); scale_log2 is then c * log2(e)
     float cap_in;            // sm_scale / c
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *queue = reinterpret_cast<const int32_t *>(p.ws + p.off_queue);
     const bsp_work_item *items = reinterpret_cast<const bsp_work_item *>(p.ws + p.off_items);
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the merge kernel may get resident now
-    const int it0 = queue[blockIdx.x], it1 = queue[blockIdx.x + 1];
+    const int qb = blockIdx.x * p.queues_per_cta;
+    const int it0 = queue[qb], it1 = queue[min(qb + p.queues_per_cta, p.num_queues)];
     if (it0 >= it1) return;  // uniform across the CTA, before any barrier
 
     auto bar = [&](int i) { return sb + kOffBar + 8u * i; };
@@ -654,7 +656,14 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill smem attribute: ") + cudaGetErrorString(e));
         configured[which][dev] = true;
     }
-    kern<<<plan->capacity.num_ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return fail(BSP_ERR_CUDA, "no current CUDA device");
+    // more plan queues than SMs: each CTA runs several consecutive queues (one wave)
+    p.num_queues = plan->capacity.num_ctas;
+    p.queues_per_cta = (p.num_queues + sms - 1) / sms;
+    const int grid = (p.num_queues + p.queues_per_cta - 1) / p.queues_per_cta;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
     return BSP_OK;
