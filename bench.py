@@ -466,7 +466,47 @@ def secondary(bsp, dev, args, pk):
     del b, pa
     torch.cuda.empty_cache()
     res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
+    res["fp8_kv_decode"] = fp8_decode(bsp, dev, steps, warm, pk)
     return res
+
+
+def fp8_decode(bsp, dev, steps, warm, pk):
+    """The batched decode workload with e4m3 K / V pools (one scale each):
+    algorithmic bytes as for bf16 but one byte per K / V element."""
+    import workloads
+    b = workloads.batched_decode_bf16()
+    f8 = workloads.fp8_kv(b)
+    pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
+                            torch.bfloat16, max_batch=b.batch, device=dev)
+    pa.plan(b.kv_indptr, b.last_page_len)
+    q = b.q.to(dev)
+    k = f8.k8.to(dev).view(torch.float8_e4m3fn)
+    v = f8.v8.to(dev).view(torch.float8_e4m3fn)
+    idx = torch.from_numpy(np.ascontiguousarray(b.kv_indices, np.int32)).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+
+    def run():
+        pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, k_scale=f8.k_scale, v_scale=f8.v_scale)
+    for _ in range(warm):
+        run()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(steps):
+        run()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    kv_tokens = int(b.kv_lens.sum())
+    nbytes = decode_bytes(b) - kv_tokens * b.num_kv_heads * b.head_dim * 2 * (esize(b) - 1)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del pa, q, k, v
+    torch.cuda.empty_cache()
+    return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
+            "bytes": nbytes, "tokens_per_s": round(b.batch / (ms * 1e-3), 1),
+            "workload": "batched decode (64 requests, KV ~ U{512..8192}, page 16 permuted, 32/8 heads, D 128), "
+                        "K / V e4m3 with one scale per pool, q / o bf16; one launch per step"}
 
 
 def vector_sparse_prefill(bsp, dev, steps, warm, pk):

@@ -30,7 +30,7 @@ _ERR_NAMES = {BSP_ERR_INVALID_ARG: "INVALID_ARG", BSP_ERR_CAPACITY: "CAPACITY", 
               BSP_ERR_UNSUPPORTED: "UNSUPPORTED", BSP_ERR_DEVICE_CHECK: "DEVICE_CHECK"}
 
 EXPORTED = ["bsp_default_num_ctas", "bsp_workspace_size", "bsp_host_staging_size", "bsp_plan",
-            "bsp_decode_run", "bsp_prefill_run", "bsp_run_attention", "bsp_run_merge_partials",
+            "bsp_decode_run", "bsp_decode_run_fp8", "bsp_prefill_run", "bsp_run_attention", "bsp_run_merge_partials",
             "bsp_merge_state", "bsp_decode_run_static", "bsp_check_device_error",
             "bsp_last_error", "bsp_version"]
 
@@ -94,6 +94,7 @@ def load():
         "bsp_host_staging_size": ([P, C], ctypes.c_size_t),
         "bsp_plan": ([P, C, i32, vp, vp, vp, i64, i64, vp, vp, ctypes.c_size_t, vp, PI], ctypes.c_int),
         "bsp_decode_run": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
+        "bsp_decode_run_fp8": ([PI, vp, vp, vp, vp, i64, f32, f32, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_prefill_run": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_run_attention": ([PI, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp], ctypes.c_int),
         "bsp_run_merge_partials": ([PI, vp, vp, vp, vp], ctypes.c_int),

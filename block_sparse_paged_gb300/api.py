@@ -149,7 +149,10 @@ class PagedAttention:
     # ---- run ----------------------------------------------------------------
     def run(self, q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, kv_indices: torch.Tensor,
             sm_scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            stream=None, return_lse: bool = True):
+            stream=None, return_lse: bool = True, k_scale: float = 1.0, v_scale: float = 1.0):
+        """Attention of the planned batch. k_pages / v_pages are in the
+        problem's dtype, or, for bf16 decode, torch.float8_e4m3fn pools read as
+        k_scale * k_pages and v_scale * v_pages (one scale per pool)."""
         if self.info is None:
             raise RuntimeError("plan() must be called before run()")
         P = self.problem
@@ -165,15 +168,24 @@ class PagedAttention:
         if lse is None and return_lse:
             lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
         dev = self.device
-        args = [ctypes.byref(self.info), _dev(q, "q", self.dtype, dev), _dev(k_pages, "k_pages", self.dtype, dev),
-                _dev(v_pages, "v_pages", self.dtype, dev), _dev(kv_indices, "kv_indices", torch.int32, dev)
+        fp8 = k_pages.dtype == torch.float8_e4m3fn
+        if fp8 and (self.mode != N.BSP_MODE_DECODE or self.dtype != torch.bfloat16):
+            raise ValueError("e4m3 KV pools are read by the bf16 decode run only")
+        kv_dt = torch.float8_e4m3fn if fp8 else self.dtype
+        if not fp8 and (k_scale != 1.0 or v_scale != 1.0):
+            raise ValueError("k_scale / v_scale apply to e4m3 KV pools only")
+        args = [ctypes.byref(self.info), _dev(q, "q", self.dtype, dev), _dev(k_pages, "k_pages", kv_dt, dev),
+                _dev(v_pages, "v_pages", kv_dt, dev), _dev(kv_indices, "kv_indices", torch.int32, dev)
                 if kv_indices.numel() else None]
         tail = [ctypes.c_float(sm_scale), _dev(out, "out", self.dtype, dev),
                 None if lse is None else _dev(lse, "lse", torch.float32, dev),
                 ctypes.c_void_p(self.workspace.data_ptr())]
         with torch.cuda.device(dev):
             s = _stream_handle(stream)
-            if self.mode == N.BSP_MODE_DECODE:
+            if fp8:
+                N.check(self.lib.bsp_decode_run_fp8(*args, k_pages.shape[0], tail[0], ctypes.c_float(k_scale),
+                                                    ctypes.c_float(v_scale), *tail[1:], s))
+            elif self.mode == N.BSP_MODE_DECODE:
                 N.check(self.lib.bsp_decode_run(*args, k_pages.shape[0], *tail, s))
             else:
                 N.check(self.lib.bsp_prefill_run(*args, k_pages.shape[0], *tail, s))

@@ -74,6 +74,18 @@ extern "C" int bsp_decode_run(const bsp_plan_info *plan, const void *q, const vo
     return launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
 }
 
+extern "C" int bsp_decode_run_fp8(const bsp_plan_info *plan, const void *q, const void *k_pages,
+                                  const void *v_pages, const int32_t *kv_indices, int64_t num_pages, float sm_scale,
+                                  float k_scale, float v_scale, void *o, float *lse, void *workspace,
+                                  bsp_stream_t stream) {
+    clear_error();
+    int rc = check_plan(plan, BSP_MODE_DECODE, workspace);
+    if (rc != BSP_OK) return rc;
+    if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    return launch_decode_fp8(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, k_scale, v_scale, o, lse,
+                             workspace, stream);
+}
+
 extern "C" int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
                                const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
                                void *workspace, bsp_stream_t stream) {

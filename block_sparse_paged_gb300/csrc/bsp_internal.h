@@ -59,11 +59,19 @@ inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 // BSP_ERR_* (unaligned base, encoder unavailable or rejecting the shape).
 int make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t dim, uint64_t heads, uint64_t rows, uint32_t box_heads,
                    uint32_t box_rows);
+// The same for 1- or 2-byte elements: boxes of 128 / elem_bytes elements (one
+// 128-byte swizzle row) x box_heads x box_rows.
+int make_tmap(CUtensorMap *map, const void *base, int elem_bytes, uint64_t dim, uint64_t heads, uint64_t rows,
+              uint32_t box_heads, uint32_t box_rows);
 
 // Launchers (defined in the .cu files). They return BSP_OK or BSP_ERR_*.
 int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
                   const void *v_pages, const int32_t *kv_indices, int64_t num_pages, float sm_scale,
                   void *o, float *lse, void *workspace, cudaStream_t stream);
+// Decode over e4m3 K/V pools with per-tensor scales (bf16 q and o).
+int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *kv_indices, int64_t num_pages, float sm_scale, float k_scale, float v_scale,
+                      void *o, float *lse, void *workspace, cudaStream_t stream);
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages,
                    const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
                    float sm_scale, void *o, float *lse, void *workspace, cudaStream_t stream);

@@ -30,8 +30,11 @@
 // Reduction kernel: the reduction map's slots of each split output, merged in
 // ascending order with a common maximum (technical review eq 6), no atomics.
 #include <cfloat>
+#include <cmath>
 #include <climits>
 #include <cstring>
+
+#include <cuda_fp16.h>
 
 #include "bsp_internal.h"
 #include "device_common.cuh"
@@ -48,25 +51,50 @@ constexpr int kMmaRows = 16;                 // fused heads per tile (M of the M
 
 // bf16 kernel: warps 0..3 compute, warps 4 and 5 load K and V.
 constexpr int kConsumers = 4;
-constexpr int kWsThreads = 32 * (kConsumers + 2);
 constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per consumer warp)
 constexpr int kStages = 5;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 
+// Two e4m3 values (the low and high byte of the low 16 bits of x) to f16x2,
+// the low byte in the low half. Exact: every e4m3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+    uint32_t r;
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}\n" : "=r"(r) : "r"(x));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 // kTma: K and V arrive by TMA tensor copies, one per page box, as 128-byte
 // swizzled [D / 64][64 rows][128 B] tiles; otherwise by 16-byte cp.async into
 // padded rows.
-template <int D, bool kTma>
+// kFp8 (with kTma, D = 128): the ring holds e4m3 rows (128 bytes, one swizzle
+// row); the compute warps read the bytes straight into f16 tensor-core
+// fragments (no staging copy).
+template <int D, bool kTma, bool kFp8 = false>
 struct DecodeLayout {
-    static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 64-column slab
-    static constexpr int kSlab = kTma ? kTileK * 128 : 0;   // bytes per 64-column slab (TMA layout)
-    static constexpr int kTileBytes = kTma ? kTileK * D * 2 : kTileK * kPitch;  // K (or V) part of a stage
+    // kFp8: 128-token stages (half the bytes per token, so the same bytes per
+    // stage and per barrier round trip) shared by 8 compute warps, two per
+    // scheduler, so that each hides the other's latency
+    static constexpr int kTK = kFp8 ? 2 * kTileK : kTileK;   // KV tokens per stage, 16 per compute warp
+    static constexpr int kS = kStages;                       // ring stages
+    static constexpr int kCons = kTK / 16;                   // compute warps
+    static constexpr int kThreads = 32 * (kCons + 2);
+    static constexpr int kElem = kFp8 ? 1 : 2;               // bytes per K/V element in the ring
+    static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 128-byte-wide slab
+    static constexpr int kSlab = kTma ? kTK * 128 : 0;      // bytes per 128-byte-wide slab (TMA layout)
+    static constexpr int kTileBytes = kTma ? kTK * D * kElem : kTK * kPitch;  // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kScratchBytes = kConsumers * kMmaRows * D * 4;   // per-warp O rows for the item merge
-    static constexpr int kStatBytes = kConsumers * kMmaRows * 2 * 4;      // per-warp (m, l)
-    static constexpr int kBarOff = kRingBytes + kScratchBytes + kStatBytes;
-    static constexpr int kNumBars = 2 * kStages + 3;        // full[S], empty[S], merge_in, merge_out, last
+    static constexpr int kRingBytes = kS * kStageBytes;
+    static constexpr int kScratchOff = kRingBytes;
+    static constexpr int kScratchBytes = kCons * kMmaRows * D * 4;   // per-warp O rows for the item merge
+    static constexpr int kStatBytes = kCons * kMmaRows * 2 * 4;      // per-warp (m, l)
+    static constexpr int kBarOff = kScratchOff + kScratchBytes + kStatBytes;
+    static constexpr int kNumBars = 2 * kS + 3;             // full[S], empty[S], merge_in, merge_out, last
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
     // byte offset of 16-byte chunk c (of D / 8) of ring row r inside a K or V tile
@@ -91,6 +119,7 @@ struct DecodeParams {
     int window_left;         // > 0: keys j < pos + kv_len - qo_len - window_left are masked
     int soft_cap_on;         // scores: tanh(s * cap_in) * cap_out instead of s * scale_log2
     float cap_in, cap_out;   // sm_scale / c and c * log2(e)
+    float v_scale;           // output factor (per-tensor V scale of an e4m3 pool; else 1)
 };
 
 // Merge of one reduction-map entry by warps w = 0..nwarps-1 of the CTA that
@@ -154,11 +183,17 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
-template <int D, bool kTma>
-__global__ void __launch_bounds__(kWsThreads, 1)
+template <int D, bool kTma, bool kFp8 = false>
+__global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const DecodeParams p) {
-    using LY = DecodeLayout<D, kTma>;
+    static_assert(!kFp8 || (kTma && D == 128), "e4m3 pools: TMA gather, head_dim 128");
+    using LY = DecodeLayout<D, kTma, kFp8>;
+    constexpr int kStages = LY::kS;
+    constexpr int kConsumers = LY::kCons;
+    constexpr int kWsThreads = LY::kThreads;
+    constexpr int kTK = LY::kTK;
+    static_assert(kConsumers == 4 || kConsumers == 8, "four or eight compute warps");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *smem = kTma ? smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023) : smem_raw;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -205,33 +240,43 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const CUtensorMap *map = is_v ? &tv : &tk;
         const uint32_t part = is_v ? LY::kTileBytes : 0;
         const int br = p.box_rows;
+        const int bps = kTK / br;     // boxes per stage (br is a power of two, 8..64): at most 16
+        const int spb = 32 / bps;     // stages whose page ids one warp-wide load covers
         int k = 0;
         for (int it = it0; it < it1 && !*abort_flag; ++it) {
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
-            const int nt = (len + kTileK - 1) / kTileK;
-            auto fetch = [&](int t) -> int {  // page id of this lane's box in stage t
-                const int r = t * kTileK + lane * br;
-                return (lane * br < kTileK && r < len) ? __ldg(p.kv_indices + w.page_base + (w.kv_start + r) / p.page_size)
-                                                       : 0;
+            const int nt = (len + kTK - 1) / kTK;
+            // Page ids come in batches of 32 (lane l: box l % bps of stage l / bps of
+            // the batch), one batch ahead, so that their latency under a full
+            // memory system overlaps the copies instead of gating every stage.
+            auto fetch_batch = [&](int b) -> int {
+                const int r = (b * spb + lane / bps) * kTK + (lane % bps) * br;
+                return r < len ? __ldg(p.kv_indices + w.page_base + (w.kv_start + r) / p.page_size) : 0;
             };
-            int pg = nt > 0 ? fetch(0) : 0;
+            int cur = nt > 0 ? fetch_batch(0) : 0;
+            int nxt = spb < nt ? fetch_batch(1) : 0;
             for (int t = 0; t < nt; ++t, ++k) {
-                const int n = min(kTileK, len - t * kTileK);
+                if (t > 0 && t % spb == 0) {
+                    cur = nxt;
+                    if (t + spb < nt) nxt = fetch_batch(t / spb + 1);
+                }
+                const int pg = __shfl_sync(0xffffffffu, cur, (t % spb) * bps + (lane < bps ? lane : 0));
+                const int n = min(kTK, len - t * kTK);
                 const int nbox = (n + br - 1) / br;
-                const int row0 = pg * p.page_size + (w.kv_start + t * kTileK + lane * br) % p.page_size;
-                if (t + 1 < nt) pg = fetch(t + 1);
+                const int row0 = pg * p.page_size + (w.kv_start + t * kTK + lane * br) % p.page_size;
                 const int s = k % kStages;
                 const bool ok = wait_or_abort(empty0 + 8 * s, ((k / kStages) & 1) ^ 1, abort_flag, status,
                                               kStatusProducerWait);
                 if (!__all_sync(0xffffffffu, ok)) break;
-                if (lane == 0) sm100::mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nbox * br * D * 2));
+                if (lane == 0) sm100::mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nbox * br * D * LY::kElem));
                 __syncwarp();
                 if (lane < nbox) {
                     const uint32_t dst = sbase + s * LY::kStageBytes + part + (uint32_t)(lane * br * 128);
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        sm100::tma_load_3d(dst + h * LY::kSlab, map, full0 + 8 * s, h * 64, w.kv_head, row0);
+                    for (int h = 0; h < D * LY::kElem / 128; ++h)  // one copy per 128-byte-wide slab
+                        sm100::tma_load_3d(dst + h * LY::kSlab, map, full0 + 8 * s, h * (128 / LY::kElem), w.kv_head,
+                                           row0);
                 }
             }
         }
@@ -296,14 +341,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // ---------------- consumers: warps 0..3 ----------------------------------
     const int g = p.g;
     const int r0 = lane >> 2, r1 = r0 + 8;
-    float *scratch = reinterpret_cast<float *>(smem + LY::kRingBytes);                       // [warp][16][D]
-    float *stats = reinterpret_cast<float *>(smem + LY::kRingBytes + LY::kScratchBytes);   // [warp][16][m, l]
+    float *scratch = reinterpret_cast<float *>(smem + LY::kScratchOff);                      // [warp][16][D]
+    float *stats = reinterpret_cast<float *>(smem + LY::kScratchOff + LY::kScratchBytes);  // [warp][16][m, l]
     int k = 0, merges = 0, lasts = 0;
     bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
     for (int it = it0; it < it1; ++it) {
         const bsp_work_item w = items[it];
         const int len = w.kv_end - w.kv_start;
-        const int nt = (len + kTileK - 1) / kTileK;
+        const int nt = (len + kTK - 1) / kTK;
 
         // Q fragments of the g fused rows (rows >= g are zero)
         uint32_t qa[D / 16][4];
@@ -312,6 +357,22 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                       ((size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g) * D;
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(qb + (size_t)r0 * D);
             const uint32_t *q1 = reinterpret_cast<const uint32_t *>(qb + (size_t)r1 * D);
+            if constexpr (kFp8) {
+                // f16 fragments (exact for bf16 values of magnitude 2^-14 .. 65504;
+                // larger ones saturate) in the dimension order of the e4m3 K
+                // fragments: step kk = 4h + j covers dims 64h + 16c + 4j + {0..3}
+                // for the lane's column pair c, split {0, 1} and {2, 3}
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c2 = (64 * (kk >> 2) + 16 * (lane & 3) + 4 * (kk & 3)) >> 1;
+                    const uint32_t x0 = r0 < g ? __ldg(q0 + c2) : 0u, x1 = r1 < g ? __ldg(q1 + c2) : 0u;
+                    const uint32_t y0 = r0 < g ? __ldg(q0 + c2 + 1) : 0u, y1 = r1 < g ? __ldg(q1 + c2 + 1) : 0u;
+                    qa[kk][0] = pack_f16_sat(bf16_lo(x0), bf16_hi(x0));
+                    qa[kk][1] = pack_f16_sat(bf16_lo(x1), bf16_hi(x1));
+                    qa[kk][2] = pack_f16_sat(bf16_lo(y0), bf16_hi(y0));
+                    qa[kk][3] = pack_f16_sat(bf16_lo(y1), bf16_hi(y1));
+                }
+            } else
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c2 = (kk * 16 + 2 * (lane & 3)) >> 1;  // index in bf16 pairs
@@ -330,20 +391,46 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int s = k % kStages;
             const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
             if (!__all_sync(0xffffffffu, ok)) return;
-            const int valid = min(kTileK, len - t * kTileK) - warp * 16;  // this warp's tokens
+            const int quarter = warp;                                   // 16-token slice of the stage
+            const int valid = min(kTK, len - t * kTK) - quarter * 16;  // this warp's tokens
             // sliding window: tokens of this warp before the window's edge (the chunk
             // starts on a page boundary at or before it) are masked
             const int lo_rel = p.window_left > 0
-                                   ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTileK + warp * 16)
+                                   ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + quarter * 16)
                                    : INT_MIN;
+            bool released = false;
             if (valid > 0) {
-                const uint32_t kb = sbase + s * LY::kStageBytes;
-                const uint32_t vb = kb + LY::kTileBytes;
-                if (kTma && valid < 16) {
+                uint32_t kb = sbase + s * LY::kStageBytes;
+                uint32_t vb = kb + LY::kTileBytes;
+                uint4 kw[2][2], vw[4];
+                if constexpr (kFp8) {
+                    // e4m3 bytes straight into registers. K: tile t, half h -> row
+                    // 8t + (lane >> 2) of this warp, dims 64h + 16c .. + 15.
+                    // V: rows 2c, 2c + 1, 2c + 8, 2c + 9 (the P columns this lane
+                    // holds), dims 16 (lane >> 2) .. + 15, zero past the chunk end.
+                    const int c = lane & 3, qn = lane >> 2;
+#pragma unroll
+                    for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int R = quarter * 16 + 8 * t2 + qn;
+                            kw[t2][h] = sm100::ld_shared_v4(kb + R * 128 + (((4 * h + c) ^ (R & 7)) << 4));
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = quarter * 16 + rr;
+                        vw[i] = sm100::ld_shared_v4(vb + R * 128 + ((qn ^ (R & 7)) << 4));
+                        if (rr >= valid) vw[i] = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                    if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);  // the stage is in registers
+                    released = true;
+                }
+                if (kTma && !kFp8 && valid < 16) {
                     // whole page boxes were copied: V rows of this warp past the chunk
                     // end may hold anything; zero them so that P = 0 meets finite values
                     for (int e = lane; e < (16 - valid) * (D / 8); e += 32) {
-                        const int row = warp * 16 + valid + e / (D / 8);
+                        const int row = quarter * 16 + valid + e / (D / 8);
                         *reinterpret_cast<uint4 *>(smem + (vb - sbase) + LY::chunk(row, e % (D / 8))) =
                             make_uint4(0, 0, 0, 0);
                     }
@@ -352,9 +439,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 float sc[2][4];
 #pragma unroll
                 for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-                {
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+                        for (int t2 = 0; t2 < 2; ++t2) {
+                            const uint4 &v4 = kw[t2][kk >> 2];
+                            const uint32_t wd = (kk & 3) == 0 ? v4.x : (kk & 3) == 1 ? v4.y : (kk & 3) == 2 ? v4.z : v4.w;
+                            mma_f16_16816(sc[t2], qa[kk], e4m3x2_to_f16x2(wd), e4m3x2_to_f16x2(wd >> 16));
+                        }
+                    }
+                } else {
                     const int mi = lane >> 3;
-                    const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+                    const int row = quarter * 16 + (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         uint32_t b0, b1, b2, b3;
@@ -406,13 +503,35 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                 }
                 uint32_t pa[4];
+                if constexpr (kFp8) {
+                    pa[0] = pack_f16_sat(ps[0][0], ps[0][1]);
+                    pa[1] = pack_f16_sat(ps[0][2], ps[0][3]);
+                    pa[2] = pack_f16_sat(ps[1][0], ps[1][1]);
+                    pa[3] = pack_f16_sat(ps[1][2], ps[1][3]);
+                    // tile nd, column n of the output holds dim 16 n + nd: this lane's
+                    // V bytes (dims 16 (lane >> 2) + 4m .. + 3) pair up token rows
+                    // (2c, 2c + 1) and (2c + 8, 2c + 9) byte by byte
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t a = m == 0 ? vw[0].x : m == 1 ? vw[0].y : m == 2 ? vw[0].z : vw[0].w;
+                        const uint32_t b = m == 0 ? vw[1].x : m == 1 ? vw[1].y : m == 2 ? vw[1].z : vw[1].w;
+                        const uint32_t c8 = m == 0 ? vw[2].x : m == 1 ? vw[2].y : m == 2 ? vw[2].z : vw[2].w;
+                        const uint32_t d8 = m == 0 ? vw[3].x : m == 1 ? vw[3].y : m == 2 ? vw[3].z : vw[3].w;
+                        const uint32_t lo01 = prmt(a, b, 0x5140), lo23 = prmt(a, b, 0x7362);
+                        const uint32_t hi01 = prmt(c8, d8, 0x5140), hi23 = prmt(c8, d8, 0x7362);
+                        mma_f16_16816(acc[4 * m + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(hi01));
+                        mma_f16_16816(acc[4 * m + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
+                        mma_f16_16816(acc[4 * m + 2], pa, e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(hi23));
+                        mma_f16_16816(acc[4 * m + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+                    }
+                } else {
                 pa[0] = pack_bf16(ps[0][0], ps[0][1]);
                 pa[1] = pack_bf16(ps[0][2], ps[0][3]);
                 pa[2] = pack_bf16(ps[1][0], ps[1][1]);
                 pa[3] = pack_bf16(ps[1][2], ps[1][3]);
                 {
                     const int mi = lane >> 3;
-                    const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
+                    const int row = quarter * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
                     for (int nd = 0; nd < D / 16; ++nd) {
                         uint32_t b0, b1, b2, b3;
@@ -421,10 +540,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
                     }
                 }
+                }
             }
-            if (kTma) sm100::fence_proxy_async_smem();  // generic writes above before the next tensor copy
-            __syncwarp();
-            if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+            if (!released) {
+                if (kTma) sm100::fence_proxy_async_smem();  // generic writes above before the next tensor copy
+                __syncwarp();
+                if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+            }
         }
 
         // ---- merge the four warps' states; write the output or a partial ----
@@ -438,6 +560,22 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             stats[(warp * 16 + r1) * 2 + 0] = m1;
             stats[(warp * 16 + r1) * 2 + 1] = l1;
         }
+        if constexpr (kFp8) {
+            // accumulator tile nd, column pair (2c, 2c + 1) holds dims 32c + nd and 32c + 16 + nd
+            float *s0 = scratch + (warp * 16 + r0) * D + 32 * (lane & 3);
+            float *s1 = scratch + (warp * 16 + r1) * D + 32 * (lane & 3);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                *reinterpret_cast<float4 *>(s0 + 4 * i) =
+                    make_float4(acc[4 * i][0], acc[4 * i + 1][0], acc[4 * i + 2][0], acc[4 * i + 3][0]);
+                *reinterpret_cast<float4 *>(s0 + 16 + 4 * i) =
+                    make_float4(acc[4 * i][1], acc[4 * i + 1][1], acc[4 * i + 2][1], acc[4 * i + 3][1]);
+                *reinterpret_cast<float4 *>(s1 + 4 * i) =
+                    make_float4(acc[4 * i][2], acc[4 * i + 1][2], acc[4 * i + 2][2], acc[4 * i + 3][2]);
+                *reinterpret_cast<float4 *>(s1 + 16 + 4 * i) =
+                    make_float4(acc[4 * i][3], acc[4 * i + 1][3], acc[4 * i + 2][3], acc[4 * i + 3][3]);
+            }
+        } else
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
             const int col = n * 8 + 2 * (lane & 3);
@@ -461,7 +599,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     L += stats[(ww * 16 + row) * 2 + 1] * f;
                     num += scratch[(ww * 16 + row) * D + d] * f;
                 }
-                val = num / L;
+                val = num / L * p.v_scale;
                 lse_v = (M + log2f(L)) * kLn2;
             }
             if (w.slot < 0) {
@@ -639,19 +777,20 @@ int num_sms_of_current_device(int *dev_out) {
     return sms[dev];
 }
 
-template <int D, bool kTma>
+template <int D, bool kTma, bool kFp8 = false>
 int launch_decode_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                        cudaStream_t stream) {
     static bool configured[64] = {false};
     int dev = 0;
     if (num_sms_of_current_device(&dev) < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    constexpr int kSmem = DecodeLayout<D, kTma, kFp8>::kSmemBytes;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecodeLayout<D, kTma>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma, kFp8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
         configured[dev] = true;
     }
-    decode_bf16_kernel<D, kTma><<<grid, kWsThreads, DecodeLayout<D, kTma>::kSmemBytes, stream>>>(tk, tv, p);
+    decode_bf16_kernel<D, kTma, kFp8><<<grid, DecodeLayout<D, kTma, kFp8>::kThreads, kSmem, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
     return BSP_OK;
@@ -691,11 +830,13 @@ int decode_ctas_per_sm(int head_dim, int dtype) {
     return 1;  // a 5-stage ring of 64-token K+V stages (~174 KB at D = 128) per SM
 }
 
-int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
-                  const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
-                  void *workspace, cudaStream_t stream) {
+namespace {
+
+// Parameters shared by the bf16/fp32 and e4m3 launchers; returns the grid size.
+int decode_params(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                  const int32_t *kv_indices, float sm_scale, float k_scale, float v_scale, void *o, float *lse,
+                  void *workspace, DecodeParams &p) {
     const bsp_problem &P = plan->problem;
-    DecodeParams p;
     p.ws = static_cast<const uint8_t *>(workspace);
     p.off_queue = plan->off_queue_indptr;
     p.off_items = plan->off_items;
@@ -707,10 +848,13 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     p.kv_indices = kv_indices;
     p.o = o;
     p.lse = lse;
-    p.scale_log2 = sm_scale * kLog2e;
+    // s = sm_scale * q . (k_scale * k): the K scale folds into the score scale
+    const float qk_scale = sm_scale * k_scale;
+    p.scale_log2 = qk_scale * kLog2e;
+    p.v_scale = v_scale;
     p.window_left = P.window_left;
     p.soft_cap_on = P.logits_soft_cap > 0.f;
-    p.cap_in = p.soft_cap_on ? sm_scale / P.logits_soft_cap : 0.f;
+    p.cap_in = p.soft_cap_on ? qk_scale / P.logits_soft_cap : 0.f;
     p.cap_out = P.logits_soft_cap * kLog2e;
     p.H_qo = P.num_qo_heads;
     p.H_kv = P.num_kv_heads;
@@ -720,11 +864,22 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
     // A plan may have more queues than CTAs fit on the GPU at once: each CTA then
     // runs several consecutive queues (one wave; the planner balanced every queue).
     const int sms = num_sms_of_current_device(nullptr);
-    if (sms < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    if (sms < 0) return -1;
     const int resident = sms * decode_ctas_per_sm(P.head_dim, P.dtype);
     p.num_queues = plan->capacity.num_ctas;
     p.queues_per_cta = (p.num_queues + resident - 1) / resident;
-    const int grid = (p.num_queues + p.queues_per_cta - 1) / p.queues_per_cta;
+    return (p.num_queues + p.queues_per_cta - 1) / p.queues_per_cta;
+}
+
+}  // namespace
+
+int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                  const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
+                  void *workspace, cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    DecodeParams p;
+    const int grid = decode_params(plan, q, k_pages, v_pages, kv_indices, sm_scale, 1.f, 1.f, o, lse, workspace, p);
+    if (grid < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
     if (P.dtype == BSP_DTYPE_BF16) {
         if (p.g > kMmaRows) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode needs num_qo_heads / num_kv_heads <= 16");
         if (P.head_dim != 128 && P.head_dim != 64) return fail(BSP_ERR_UNSUPPORTED, "bf16 decode supports head_dim 64 and 128");
@@ -757,6 +912,33 @@ int launch_decode(const bsp_plan_info *plan, const void *q, const void *k_pages,
         case 256: return launch_decode_f32<256>(p, grid, stream);
         default: return fail(BSP_ERR_UNSUPPORTED, "fp32 decode supports head_dim 32, 64, 128, 256");
     }
+}
+
+int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *kv_indices, int64_t num_pages, float sm_scale, float k_scale, float v_scale,
+                      void *o, float *lse, void *workspace, cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    if (P.dtype != BSP_DTYPE_BF16 || P.head_dim != 128)
+        return fail(BSP_ERR_UNSUPPORTED, "e4m3 KV decode needs a bf16 problem (queries, outputs) with head_dim 128");
+    if (plan->group > kMmaRows) return fail(BSP_ERR_UNSUPPORTED, "e4m3 KV decode needs num_qo_heads / num_kv_heads <= 16");
+    const int ps = P.page_size;
+    if (ps < 8 || (ps & (ps - 1)) != 0)
+        return fail(BSP_ERR_UNSUPPORTED, "e4m3 KV decode needs a power-of-two page size of at least 8");
+    if (num_pages <= 0 || num_pages * (int64_t)ps > INT32_MAX)
+        return fail(BSP_ERR_INVALID_ARG, "e4m3 KV decode needs the pool size: 0 < num_pages * page_size <= 2^31 - 1");
+    if (!(std::isfinite(k_scale) && std::isfinite(v_scale)) || k_scale <= 0.f || v_scale <= 0.f)
+        return fail(BSP_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
+    DecodeParams p;
+    const int grid = decode_params(plan, q, k_pages, v_pages, kv_indices, sm_scale, k_scale, v_scale, o, lse,
+                                   workspace, p);
+    if (grid < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    p.box_rows = ps < kTileK ? ps : kTileK;
+    const uint64_t rows = (uint64_t)num_pages * ps;
+    CUtensorMap tk, tv;
+    int rc = make_tmap(&tk, k_pages, 1, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
+    if (rc == BSP_OK) rc = make_tmap(&tv, v_pages, 1, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
+    if (rc != BSP_OK) return rc;
+    return launch_decode_bf16<128, true, true>(tk, tv, p, grid, stream);
 }
 
 int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace, cudaStream_t stream) {

@@ -240,6 +240,29 @@ int bsp_decode_run(const bsp_plan_info *plan, const void *q, const void *k_pages
                    float sm_scale, void *o, float *lse, void *workspace, bsp_stream_t stream);
 
 /*
+ * Decode run over an e4m3 (FP8) KV cache (the e4m3 KV-cache configuration of
+ * FlashInfer: A Customizable Attention Engine for LLM Serving, App. G.4
+ * Table 8). Keys and values are stored as OCP e4m3 bytes with one scale per
+ * pool: k = k_scale * k8, v = v_scale * v8. Everything else is bsp_decode_run
+ * with those k and v; queries and outputs stay bf16, scores and the state are
+ * fp32, and the converted values are exact (every e4m3 value is a bf16 value).
+ *   plan        from bsp_plan with mode BSP_MODE_DECODE and dtype bf16
+ *   q           device, bf16 [n_tokens, H_qo, 128]
+ *   k_pages,
+ *   v_pages     device, e4m3 bytes [num_pages, page_size, H_kv, 128]
+ *   num_pages   pages in each pool, > 0 (bounds the tensor maps)
+ *   k_scale,
+ *   v_scale     finite, > 0
+ *   o, lse, kv_indices, workspace: as for bsp_decode_run
+ * Supported: head_dim 128, g <= 16, page_size a power of two >= 8. Anything
+ * else is BSP_ERR_UNSUPPORTED (shape) or BSP_ERR_INVALID_ARG (scales, pool).
+ */
+int bsp_decode_run_fp8(const bsp_plan_info *plan, const void *q, const void *k_pages,
+                       const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
+                       float sm_scale, float k_scale, float v_scale, void *o, float *lse,
+                       void *workspace, bsp_stream_t stream);
+
+/*
  * Prefill run: ragged queries, tiles of 256 packed rows (positions x g heads,
  * technical review eq 3) against KV tiles gathered page by page into shared
  * memory, QK^T and PV on the tensor cores (sparse gather, dense compute:

@@ -7,6 +7,7 @@ do. It shares no code with the CUDA path.
 - ``attention.c``: the attention definition and the exact state merge, in C,
   fp64, one output at a time (loaded here through ctypes).
 - ``plan.py``: the load-balanced plan in plain Python.
+- ``fp8.py``: values of e4m3 KV codes (for the e4m3 KV-cache decode).
 
 ``build()`` compiles ``attention.c`` with gcc into ``liboracle.so`` next to it.
 """
@@ -18,6 +19,7 @@ import subprocess
 
 import numpy as np
 
+from . import fp8 as fp8  # noqa: F401  (re-export)
 from . import plan as plan  # noqa: F401  (re-export)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -158,10 +160,11 @@ def merge_states(*a, **k):
     return default().merge_states(*a, **k)
 
 
-def attention_of(batch, num_threads: int = 0, **kw):
-    """All outputs of a workloads.PagedBatch."""
-    return default().attention(batch.q.float().numpy(), batch.k_pages.float().numpy(),
-                               batch.v_pages.float().numpy(), batch.qo_indptr, batch.kv_indptr,
+def attention_of(batch, num_threads: int = 0, k=None, v=None, **kw):
+    """All outputs of a workloads.PagedBatch (K / V value arrays may be passed in)."""
+    k = batch.k_pages.float().numpy() if k is None else k
+    v = batch.v_pages.float().numpy() if v is None else v
+    return default().attention(batch.q.float().numpy(), k, v, batch.qo_indptr, batch.kv_indptr,
                                batch.kv_indices, batch.last_page_len, batch.num_qo_heads,
                                batch.num_kv_heads, batch.page_size, batch.causal, batch.sm_scale,
                                num_threads=num_threads, window_left=getattr(batch, "window_left", -1),

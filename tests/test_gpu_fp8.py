@@ -1,0 +1,104 @@
+"""Decode over an e4m3 KV cache (FlashInfer: A Customizable Attention Engine
+for LLM Serving, App. G.4 Table 8, the e4m3 rows) against the oracle run on
+the values the codes stand for (oracle.fp8: k_scale * value(code))."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import compare, lib, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    return lib()
+
+
+def run_fp8(bsp, b, f8, num_ctas=None, repeats=1):
+    pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
+                            torch.bfloat16, max_batch=b.batch, num_ctas=num_ctas, window_left=b.window_left,
+                            logits_soft_cap=b.soft_cap)
+    pa.plan(b.kv_indptr, b.last_page_len)
+    q = b.q.cuda()
+    k = f8.k8.cuda().view(torch.float8_e4m3fn)
+    v = f8.v8.cuda().view(torch.float8_e4m3fn)
+    idx = torch.from_numpy(np.ascontiguousarray(b.kv_indices, np.int32)).cuda()
+    for _ in range(repeats):
+        out, lse = pa.run(q, k, v, idx, b.sm_scale, k_scale=f8.k_scale, v_scale=f8.v_scale)
+    torch.cuda.synchronize()
+    return out, lse, pa
+
+
+def oracle_kv(f8):
+    return (oracle.fp8.dequantize(f8.k8.numpy(), f8.k_scale), oracle.fp8.dequantize(f8.v8.numpy(), f8.v_scale))
+
+
+CASES = [
+    # (seed, kv lens, H_qo, H_kv, page, num_ctas, window, cap)
+    (101, [3000, 17, 900, 4100, 1, 250, 64, 65], 32, 8, 16, 29, -1, 0.0),   # splits, ragged tails
+    (102, [5000, 33, 129], 32, 8, 8, 17, -1, 0.0),                         # page 8 (box of 8 rows)
+    (103, [2048, 1000, 7], 16, 4, 32, 11, -1, 0.0),
+    (104, [4000, 300], 64, 8, 64, 9, -1, 0.0),                             # g = 8, page 64
+    (105, [6000, 130, 2], 32, 2, 128, 23, -1, 0.0),                        # g = 16, page 128 (two boxes)
+    (106, [3000, 900, 4100], 32, 8, 16, 13, 700, 1.5),                     # window and soft-cap
+    (107, [0, 40, 0, 1], 32, 8, 16, 5, -1, 0.0),                           # empty requests
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"fp8_{c[0]}" for c in CASES])
+def test_fp8_decode(bsp, case):
+    seed, kv, hq, hk, ps, C, w, cap = case
+    b = workloads.paged_batch(seed, [1] * len(kv), kv, hq, hk, 128, ps, "bf16", extra_pages=3)
+    b.window_left, b.soft_cap = w, cap
+    f8 = workloads.fp8_kv(b)
+    kd, vd = oracle_kv(f8)
+    O, L = oracle.attention_of(b, k=kd, v=vd)
+    out, lse, pa = run_fp8(bsp, b, f8, num_ctas=C)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_fp8_scales_are_applied(bsp):
+    """Scaling K by 2 doubles every score and V by 3 triples every output: the
+    same codes with other scales against the oracle with those scales."""
+    b = workloads.paged_batch(108, [1] * 3, [700, 64, 2000], 32, 8, 128, 16, "bf16", extra_pages=1)
+    f8 = workloads.fp8_kv(b)
+    f8.k_scale *= 2.0
+    f8.v_scale *= 3.0
+    kd, vd = oracle_kv(f8)
+    O, L = oracle.attention_of(b, k=kd, v=vd)
+    out, lse, _ = run_fp8(bsp, b, f8, num_ctas=7)
+    compare(out, lse, O, L, "bf16")
+
+
+def test_fp8_full_size_decode(bsp):
+    """The Llama-3-8B-shaped batched decode (batch 64, KV up to 8192, page 16)
+    with e4m3 K / V: sampled rows against the oracle; run twice on one plan
+    (the in-kernel merge resets its counters)."""
+    b = workloads.batched_decode_bf16()
+    f8 = workloads.fp8_kv(b)
+    out, lse, pa = run_fp8(bsp, b, f8, repeats=2)
+    tok, head = sample_rows(b, 256, 31)
+    kd = oracle.fp8.dequantize(f8.k8.numpy(), f8.k_scale).astype(np.float32)
+    vd = oracle.fp8.dequantize(f8.v8.numpy(), f8.v_scale).astype(np.float32)
+    # float32 copies of the fp64 values: e4m3 * scale rounds once, far below the bounds
+    O, L = oracle.attention_rows_of(b, tok, head, k_f32=kd, v_f32=vd)
+    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    assert pa.check_device_error() == 0
+
+
+def test_fp8_rejects_bad_scales_and_shapes(bsp):
+    b = workloads.paged_batch(109, [1, 1], [100, 50], 32, 8, 128, 16, "bf16")
+    f8 = workloads.fp8_kv(b)
+    f8.k_scale = 0.0
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        run_fp8(bsp, b, f8)
+    b64 = workloads.paged_batch(110, [1, 1], [100, 50], 32, 8, 64, 16, "bf16")
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        run_fp8(bsp, b64, workloads.fp8_kv(b64))
+    b4 = workloads.paged_batch(111, [1, 1], [100, 50], 32, 8, 128, 4, "bf16")
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        run_fp8(bsp, b4, workloads.fp8_kv(b4))

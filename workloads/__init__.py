@@ -332,3 +332,27 @@ WORKLOADS = {
 
 def scaled(batch: PagedBatch, **changes) -> PagedBatch:
     return replace(batch, **changes)
+
+
+@dataclass
+class Fp8KV:
+    """An e4m3 copy of a batch's K / V pools: k = k_scale * k8, v = v_scale * v8."""
+    k8: torch.Tensor   # uint8 codes (OCP e4m3), [num_pages, page_size, H_kv, D]
+    v8: torch.Tensor
+    k_scale: float
+    v_scale: float
+
+
+def fp8_kv(batch: PagedBatch) -> Fp8KV:
+    """Per-pool scale = (largest finite |x|) / 448, the e4m3 maximum; values are
+    divided by it in float32 and rounded to e4m3 by torch (nearest even,
+    saturating casts are not used: |x / scale| <= 448 already). NaN poison
+    stays NaN (code 0x7f / 0xff)."""
+    out = []
+    for t in (batch.k_pages, batch.v_pages):
+        x = t.float()
+        amax = float(torch.nan_to_num(x, nan=0.0).abs().max())
+        scale = amax / 448.0 if amax > 0 else 1.0
+        q = (x / scale).to(torch.float8_e4m3fn)
+        out += [q.view(torch.uint8).contiguous(), scale]
+    return Fp8KV(k8=out[0], v8=out[2], k_scale=out[1], v_scale=out[3])
