@@ -63,6 +63,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
     return r;
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit values held as one register per lane
+// (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -183,7 +191,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
-template <int D, bool kTma, bool kFp8 = false>
+// kNH (e4m3 only): 8-head tiles per kv head, ceil(g / 8)
+template <int D, bool kTma, bool kFp8 = false, int kNH = 1>
 __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const DecodeParams p) {
@@ -350,237 +359,316 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
         const int len = w.kv_end - w.kv_start;
         const int nt = (len + kTK - 1) / kTK;
 
-        // Q fragments of the g fused rows (rows >= g are zero)
-        uint32_t qa[D / 16][4];
-        {
-            const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q) +
-                                      ((size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g) * D;
-            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(qb + (size_t)r0 * D);
-            const uint32_t *q1 = reinterpret_cast<const uint32_t *>(qb + (size_t)r1 * D);
-            if constexpr (kFp8) {
-                // f16 fragments (exact for bf16 values of magnitude 2^-14 .. 65504;
-                // larger ones saturate) in the dimension order of the e4m3 K
-                // fragments: step kk = 4h + j covers dims 64h + 16c + 4j + {0..3}
-                // for the lane's column pair c, split {0, 1} and {2, 3}
+        if constexpr (kFp8) {
+            // e4m3 KV, transposed tiles: S^T = K Q^T and O^T = V^T P^T, so that the
+            // 16 tokens of a warp fill the M side of each MMA and the g heads the
+            // N side (8 per tile). Dimension order inside the tiles is permuted to
+            // match how a lane reads e4m3 bytes (16 at a time):
+            //   S^T step kk = 4h + j: k pairs (2c, 2c+1), (2c+8, 2c+9) are dims
+            //     64h + 16c + 4j + {0, 1} and {2, 3};
+            //   O^T tile dt: rows r and r + 8 are dims 16r + 2dt and 16r + 2dt + 1.
+            const int c = lane & 3, qn = lane >> 2;
+            uint32_t qf[D / 16][kNH][2];  // Q^T fragments, f16 (exact for bf16 values 2^-14 .. 65504; larger saturate)
+            {
+                const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q) +
+                                          ((size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g) * D;
+#pragma unroll
+                for (int nh = 0; nh < kNH; ++nh) {
+                    const int head = 8 * nh + qn;
+                    const uint32_t *qr = reinterpret_cast<const uint32_t *>(qb + (size_t)head * D);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int c2 = (64 * (kk >> 2) + 16 * c + 4 * (kk & 3)) >> 1;  // index in bf16 pairs
+                        const uint32_t x = head < g ? __ldg(qr + c2) : 0u, y = head < g ? __ldg(qr + c2 + 1) : 0u;
+                        qf[kk][nh][0] = pack_f16_sat(bf16_lo(x), bf16_hi(x));
+                        qf[kk][nh][1] = pack_f16_sat(bf16_lo(y), bf16_hi(y));
+                    }
+                }
+            }
+            // per head (2c, 2c + 1 of each 8-head tile): running max, this lane's share
+            // of the sum (its tokens r, r + 8), O^T accumulators
+            float mh[kNH][2], lh[kNH][2], oacc[D / 16][kNH][4];
+#pragma unroll
+            for (int nh = 0; nh < kNH; ++nh) {
+                mh[nh][0] = mh[nh][1] = -INFINITY;
+                lh[nh][0] = lh[nh][1] = 0.f;
+#pragma unroll
+                for (int dt = 0; dt < D / 16; ++dt) oacc[dt][nh][0] = oacc[dt][nh][1] = oacc[dt][nh][2] = oacc[dt][nh][3] = 0.f;
+            }
+
+            for (int t = 0; t < nt; ++t, ++k) {
+                const int s = k % kStages;
+                const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
+                if (!__all_sync(0xffffffffu, ok)) return;
+                const int valid = min(kTK, len - t * kTK) - warp * 16;  // this warp's tokens
+                const int lo_rel = p.window_left > 0
+                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + warp * 16)
+                                       : INT_MIN;
+                if (valid <= 0) {
+                    __syncwarp();
+                    if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+                    continue;
+                }
+                const uint32_t kb = sbase + s * LY::kStageBytes, vb = kb + LY::kTileBytes;
+                // K rows r, r + 8 (dims 64h + 16c .. + 15); V rows 2c, 2c + 1, 2c + 8,
+                // 2c + 9 (dims 16r .. + 15), zero past the chunk end; then the stage is free
+                uint4 kw[2][2], vw[4];
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int R = warp * 16 + 8 * t2 + qn;
+                        kw[t2][h] = sm100::ld_shared_v4(kb + R * 128 + (((4 * h + c) ^ (R & 7)) << 4));
+                    }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = warp * 16 + rr;
+                    vw[i] = sm100::ld_shared_v4(vb + R * 128 + ((qn ^ (R & 7)) << 4));
+                    if (rr >= valid) vw[i] = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+                if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+
+                // S^T: two accumulators per head tile (even / odd kk) to halve the chain
+                float st[kNH][2][4];
+#pragma unroll
+                for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) st[nh][e][0] = st[nh][e][1] = st[nh][e][2] = st[nh][e][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const int c2 = (64 * (kk >> 2) + 16 * (lane & 3) + 4 * (kk & 3)) >> 1;
-                    const uint32_t x0 = r0 < g ? __ldg(q0 + c2) : 0u, x1 = r1 < g ? __ldg(q1 + c2) : 0u;
-                    const uint32_t y0 = r0 < g ? __ldg(q0 + c2 + 1) : 0u, y1 = r1 < g ? __ldg(q1 + c2 + 1) : 0u;
-                    qa[kk][0] = pack_f16_sat(bf16_lo(x0), bf16_hi(x0));
-                    qa[kk][1] = pack_f16_sat(bf16_lo(x1), bf16_hi(x1));
-                    qa[kk][2] = pack_f16_sat(bf16_lo(y0), bf16_hi(y0));
-                    qa[kk][3] = pack_f16_sat(bf16_lo(y1), bf16_hi(y1));
+                    const int h = kk >> 2, j = kk & 3;
+                    const uint32_t w0 = j == 0 ? kw[0][h].x : j == 1 ? kw[0][h].y : j == 2 ? kw[0][h].z : kw[0][h].w;
+                    const uint32_t w1 = j == 0 ? kw[1][h].x : j == 1 ? kw[1][h].y : j == 2 ? kw[1][h].z : kw[1][h].w;
+                    const uint32_t a[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                                           e4m3x2_to_f16x2(w1 >> 16)};
+#pragma unroll
+                    for (int nh = 0; nh < kNH; ++nh) mma_f16_16816(st[nh][kk & 1], a, qf[kk][nh][0], qf[kk][nh][1]);
                 }
-            } else
+                // scale, mask (token r: values 0, 1; token r + 8: values 2, 3), per-head max
+                uint32_t pb[kNH][2];
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int c2 = (kk * 16 + 2 * (lane & 3)) >> 1;  // index in bf16 pairs
-                qa[kk][0] = r0 < g ? __ldg(q0 + c2) : 0u;
-                qa[kk][1] = r1 < g ? __ldg(q1 + c2) : 0u;
-                qa[kk][2] = r0 < g ? __ldg(q0 + c2 + 4) : 0u;
-                qa[kk][3] = r1 < g ? __ldg(q1 + c2 + 4) : 0u;
+                for (int nh = 0; nh < kNH; ++nh) {
+                    float sv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float v = st[nh][0][e] + st[nh][1][e];
+                        const int tk = qn + 8 * (e >> 1);
+                        const float x = p.soft_cap_on ? tanh_ex2(v * p.cap_in) * p.cap_out : v * p.scale_log2;
+                        sv[e] = (tk < valid && tk >= lo_rel) ? x : -INFINITY;
+                    }
+                    float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    const float n0 = fmaxf(mh[nh][0], mx0), n1 = fmaxf(mh[nh][1], mx1);
+                    const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+                    const float a0 = exp2f(mh[nh][0] - ref0), a1 = exp2f(mh[nh][1] - ref1);
+                    mh[nh][0] = n0;
+                    mh[nh][1] = n1;
+                    const float p0 = exp2f(sv[0] - ref0), p1 = exp2f(sv[1] - ref1);
+                    const float p2 = exp2f(sv[2] - ref0), p3 = exp2f(sv[3] - ref1);
+                    lh[nh][0] = lh[nh][0] * a0 + (p0 + p2);
+                    lh[nh][1] = lh[nh][1] * a1 + (p1 + p3);
+                    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                        for (int dt = 0; dt < D / 16; ++dt) {
+                            oacc[dt][nh][0] *= a0; oacc[dt][nh][1] *= a1;
+                            oacc[dt][nh][2] *= a0; oacc[dt][nh][3] *= a1;
+                        }
+                    }
+                    // P (tokens x heads) as two 8 x 8 f16 blocks -> transposed: P^T fragments
+                    pb[nh][0] = movmatrix_trans(pack_f16_sat(p0, p1));
+                    pb[nh][1] = movmatrix_trans(pack_f16_sat(p2, p3));
+                }
+                // O^T += V^T P^T: word m of the V rows feeds dim tiles 2m and 2m + 1
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t va = m == 0 ? vw[0].x : m == 1 ? vw[0].y : m == 2 ? vw[0].z : vw[0].w;
+                    const uint32_t vb2 = m == 0 ? vw[1].x : m == 1 ? vw[1].y : m == 2 ? vw[1].z : vw[1].w;
+                    const uint32_t vc = m == 0 ? vw[2].x : m == 1 ? vw[2].y : m == 2 ? vw[2].z : vw[2].w;
+                    const uint32_t vd = m == 0 ? vw[3].x : m == 1 ? vw[3].y : m == 2 ? vw[3].z : vw[3].w;
+                    const uint32_t lo01 = prmt(va, vb2, 0x5140), lo23 = prmt(va, vb2, 0x7362);
+                    const uint32_t hi01 = prmt(vc, vd, 0x5140), hi23 = prmt(vc, vd, 0x7362);
+                    const uint32_t a_e[4] = {e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01),
+                                             e4m3x2_to_f16x2(hi01 >> 16)};
+                    const uint32_t a_o[4] = {e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23),
+                                             e4m3x2_to_f16x2(hi23 >> 16)};
+#pragma unroll
+                    for (int nh = 0; nh < kNH; ++nh) {
+                        mma_f16_16816(oacc[2 * m][nh], a_e, pb[nh][0], pb[nh][1]);
+                        mma_f16_16816(oacc[2 * m + 1][nh], a_o, pb[nh][0], pb[nh][1]);
+                    }
+                }
             }
-        }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float acc[D / 8][4];
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-        for (int t = 0; t < nt; ++t, ++k) {
-            const int s = k % kStages;
-            const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
-            if (!__all_sync(0xffffffffu, ok)) return;
-            const int quarter = warp;                                   // 16-token slice of the stage
-            const int valid = min(kTK, len - t * kTK) - quarter * 16;  // this warp's tokens
-            // sliding window: tokens of this warp before the window's edge (the chunk
-            // starts on a page boundary at or before it) are masked
-            const int lo_rel = p.window_left > 0
-                                   ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + quarter * 16)
-                                   : INT_MIN;
-            bool released = false;
-            if (valid > 0) {
-                uint32_t kb = sbase + s * LY::kStageBytes;
-                uint32_t vb = kb + LY::kTileBytes;
-                uint4 kw[2][2], vw[4];
-                if constexpr (kFp8) {
-                    // e4m3 bytes straight into registers. K: tile t, half h -> row
-                    // 8t + (lane >> 2) of this warp, dims 64h + 16c .. + 15.
-                    // V: rows 2c, 2c + 1, 2c + 8, 2c + 9 (the P columns this lane
-                    // holds), dims 16 (lane >> 2) .. + 15, zero past the chunk end.
-                    const int c = lane & 3, qn = lane >> 2;
+            // ---- this warp's state per head -> stats / scratch rows (heads) ----
 #pragma unroll
-                    for (int t2 = 0; t2 < 2; ++t2)
+            for (int nh = 0; nh < kNH; ++nh) {
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int R = quarter * 16 + 8 * t2 + qn;
-                            kw[t2][h] = sm100::ld_shared_v4(kb + R * 128 + (((4 * h + c) ^ (R & 7)) << 4));
-                        }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = quarter * 16 + rr;
-                        vw[i] = sm100::ld_shared_v4(vb + R * 128 + ((qn ^ (R & 7)) << 4));
-                        if (rr >= valid) vw[i] = make_uint4(0, 0, 0, 0);
-                    }
-                    __syncwarp();
-                    if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);  // the stage is in registers
-                    released = true;
+                for (int o = 4; o < 32; o <<= 1) {
+                    lh[nh][0] += __shfl_xor_sync(0xffffffffu, lh[nh][0], o);
+                    lh[nh][1] += __shfl_xor_sync(0xffffffffu, lh[nh][1], o);
                 }
-                if (kTma && !kFp8 && valid < 16) {
-                    // whole page boxes were copied: V rows of this warp past the chunk
-                    // end may hold anything; zero them so that P = 0 meets finite values
-                    for (int e = lane; e < (16 - valid) * (D / 8); e += 32) {
-                        const int row = quarter * 16 + valid + e / (D / 8);
-                        *reinterpret_cast<uint4 *>(smem + (vb - sbase) + LY::chunk(row, e % (D / 8))) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    __syncwarp();
+                const int h0 = 8 * nh + 2 * c;
+                if (qn == 0) {
+                    stats[(warp * 16 + h0) * 2 + 0] = mh[nh][0];
+                    stats[(warp * 16 + h0) * 2 + 1] = lh[nh][0];
+                    stats[(warp * 16 + h0 + 1) * 2 + 0] = mh[nh][1];
+                    stats[(warp * 16 + h0 + 1) * 2 + 1] = lh[nh][1];
                 }
-                float sc[2][4];
+                float *s0 = scratch + (warp * 16 + h0) * D + 16 * qn;
+                float *s1 = s0 + D;
 #pragma unroll
-                for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-                if constexpr (kFp8) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                        for (int t2 = 0; t2 < 2; ++t2) {
-                            const uint4 &v4 = kw[t2][kk >> 2];
-                            const uint32_t wd = (kk & 3) == 0 ? v4.x : (kk & 3) == 1 ? v4.y : (kk & 3) == 2 ? v4.z : v4.w;
-                            mma_f16_16816(sc[t2], qa[kk], e4m3x2_to_f16x2(wd), e4m3x2_to_f16x2(wd >> 16));
-                        }
-                    }
-                } else {
-                    const int mi = lane >> 3;
-                    const int row = quarter * 16 + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + LY::chunk(row, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                        mma_bf16_16816(sc[1], qa[kk], b2, b3);
-                    }
-                }
-                // scale into base 2, mask tokens past the chunk end
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int tk = n * 8 + 2 * (lane & 3) + (c & 1);
-                        const float x = p.soft_cap_on ? tanh_ex2(sc[n][c] * p.cap_in) * p.cap_out : sc[n][c] * p.scale_log2;
-                        sc[n][c] = (tk < valid && tk >= lo_rel) ? x : -INFINITY;
-                    }
-                    mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-                    mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
-                const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-                m0 = n0;
-                m1 = n1;
-                float ps[2][4];
-                float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    ps[n][0] = exp2f(sc[n][0] - ref0);
-                    ps[n][1] = exp2f(sc[n][1] - ref0);
-                    ps[n][2] = exp2f(sc[n][2] - ref1);
-                    ps[n][3] = exp2f(sc[n][3] - ref1);
-                    sum0 += ps[n][0] + ps[n][1];
-                    sum1 += ps[n][2] + ps[n][3];
-                }
-                l0 = l0 * a0 + sum0;
-                l1 = l1 * a1 + sum1;
-                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-#pragma unroll
-                    for (int n = 0; n < D / 8; ++n) {
-                        acc[n][0] *= a0; acc[n][1] *= a0;
-                        acc[n][2] *= a1; acc[n][3] *= a1;
-                    }
-                }
-                uint32_t pa[4];
-                if constexpr (kFp8) {
-                    pa[0] = pack_f16_sat(ps[0][0], ps[0][1]);
-                    pa[1] = pack_f16_sat(ps[0][2], ps[0][3]);
-                    pa[2] = pack_f16_sat(ps[1][0], ps[1][1]);
-                    pa[3] = pack_f16_sat(ps[1][2], ps[1][3]);
-                    // tile nd, column n of the output holds dim 16 n + nd: this lane's
-                    // V bytes (dims 16 (lane >> 2) + 4m .. + 3) pair up token rows
-                    // (2c, 2c + 1) and (2c + 8, 2c + 9) byte by byte
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t a = m == 0 ? vw[0].x : m == 1 ? vw[0].y : m == 2 ? vw[0].z : vw[0].w;
-                        const uint32_t b = m == 0 ? vw[1].x : m == 1 ? vw[1].y : m == 2 ? vw[1].z : vw[1].w;
-                        const uint32_t c8 = m == 0 ? vw[2].x : m == 1 ? vw[2].y : m == 2 ? vw[2].z : vw[2].w;
-                        const uint32_t d8 = m == 0 ? vw[3].x : m == 1 ? vw[3].y : m == 2 ? vw[3].z : vw[3].w;
-                        const uint32_t lo01 = prmt(a, b, 0x5140), lo23 = prmt(a, b, 0x7362);
-                        const uint32_t hi01 = prmt(c8, d8, 0x5140), hi23 = prmt(c8, d8, 0x7362);
-                        mma_f16_16816(acc[4 * m + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(hi01));
-                        mma_f16_16816(acc[4 * m + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
-                        mma_f16_16816(acc[4 * m + 2], pa, e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(hi23));
-                        mma_f16_16816(acc[4 * m + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
-                    }
-                } else {
-                pa[0] = pack_bf16(ps[0][0], ps[0][1]);
-                pa[1] = pack_bf16(ps[0][2], ps[0][3]);
-                pa[2] = pack_bf16(ps[1][0], ps[1][1]);
-                pa[3] = pack_bf16(ps[1][2], ps[1][3]);
-                {
-                    const int mi = lane >> 3;
-                    const int row = quarter * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-                    for (int nd = 0; nd < D / 16; ++nd) {
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vb + LY::chunk(row, 2 * nd + (mi >> 1)), b0, b1, b2, b3);
-                        mma_bf16_16816(acc[2 * nd], pa, b0, b1);
-                        mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
-                    }
-                }
+                for (int i = 0; i < D / 32; ++i) {
+                    *reinterpret_cast<float4 *>(s0 + 4 * i) =
+                        make_float4(oacc[2 * i][nh][0], oacc[2 * i][nh][2], oacc[2 * i + 1][nh][0], oacc[2 * i + 1][nh][2]);
+                    *reinterpret_cast<float4 *>(s1 + 4 * i) =
+                        make_float4(oacc[2 * i][nh][1], oacc[2 * i][nh][3], oacc[2 * i + 1][nh][1], oacc[2 * i + 1][nh][3]);
                 }
             }
-            if (!released) {
+        } else {
+            // Q fragments of the g fused rows (rows >= g are zero)
+            uint32_t qa[D / 16][4];
+            {
+                const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q) +
+                                          ((size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g) * D;
+                const uint32_t *q0 = reinterpret_cast<const uint32_t *>(qb + (size_t)r0 * D);
+                const uint32_t *q1 = reinterpret_cast<const uint32_t *>(qb + (size_t)r1 * D);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c2 = (kk * 16 + 2 * (lane & 3)) >> 1;  // index in bf16 pairs
+                    qa[kk][0] = r0 < g ? __ldg(q0 + c2) : 0u;
+                    qa[kk][1] = r1 < g ? __ldg(q1 + c2) : 0u;
+                    qa[kk][2] = r0 < g ? __ldg(q0 + c2 + 4) : 0u;
+                    qa[kk][3] = r1 < g ? __ldg(q1 + c2 + 4) : 0u;
+                }
+            }
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+            float acc[D / 8][4];
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+            for (int t = 0; t < nt; ++t, ++k) {
+                const int s = k % kStages;
+                const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
+                if (!__all_sync(0xffffffffu, ok)) return;
+                const int valid = min(kTK, len - t * kTK) - warp * 16;  // this warp's tokens
+                // sliding window: tokens of this warp before the window's edge (the chunk
+                // starts on a page boundary at or before it) are masked
+                const int lo_rel = p.window_left > 0
+                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + warp * 16)
+                                       : INT_MIN;
+                if (valid > 0) {
+                    const uint32_t kb = sbase + s * LY::kStageBytes;
+                    const uint32_t vb = kb + LY::kTileBytes;
+                    if (kTma && valid < 16) {
+                        // whole page boxes were copied: V rows of this warp past the chunk
+                        // end may hold anything; zero them so that P = 0 meets finite values
+                        for (int e = lane; e < (16 - valid) * (D / 8); e += 32) {
+                            const int row = warp * 16 + valid + e / (D / 8);
+                            *reinterpret_cast<uint4 *>(smem + (vb - sbase) + LY::chunk(row, e % (D / 8))) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        __syncwarp();
+                    }
+                    float sc[2][4];
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                    {
+                        const int mi = lane >> 3;
+                        const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            uint32_t b0, b1, b2, b3;
+                            ldmatrix_x4(kb + LY::chunk(row, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                            mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                            mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                        }
+                    }
+                    // scale into base 2, mask tokens past the chunk end
+                    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int tk = n * 8 + 2 * (lane & 3) + (c & 1);
+                            const float x = p.soft_cap_on ? tanh_ex2(sc[n][c] * p.cap_in) * p.cap_out : sc[n][c] * p.scale_log2;
+                            sc[n][c] = (tk < valid && tk >= lo_rel) ? x : -INFINITY;
+                        }
+                        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+                        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+                    }
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                    const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+                    const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+                    m0 = n0;
+                    m1 = n1;
+                    float ps[2][4];
+                    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) {
+                        ps[n][0] = exp2f(sc[n][0] - ref0);
+                        ps[n][1] = exp2f(sc[n][1] - ref0);
+                        ps[n][2] = exp2f(sc[n][2] - ref1);
+                        ps[n][3] = exp2f(sc[n][3] - ref1);
+                        sum0 += ps[n][0] + ps[n][1];
+                        sum1 += ps[n][2] + ps[n][3];
+                    }
+                    l0 = l0 * a0 + sum0;
+                    l1 = l1 * a1 + sum1;
+                    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                        for (int n = 0; n < D / 8; ++n) {
+                            acc[n][0] *= a0; acc[n][1] *= a0;
+                            acc[n][2] *= a1; acc[n][3] *= a1;
+                        }
+                    }
+                    uint32_t pa[4];
+                    pa[0] = pack_bf16(ps[0][0], ps[0][1]);
+                    pa[1] = pack_bf16(ps[0][2], ps[0][3]);
+                    pa[2] = pack_bf16(ps[1][0], ps[1][1]);
+                    pa[3] = pack_bf16(ps[1][2], ps[1][3]);
+                    {
+                        const int mi = lane >> 3;
+                        const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                        for (int nd = 0; nd < D / 16; ++nd) {
+                            uint32_t b0, b1, b2, b3;
+                            ldmatrix_x4_trans(vb + LY::chunk(row, 2 * nd + (mi >> 1)), b0, b1, b2, b3);
+                            mma_bf16_16816(acc[2 * nd], pa, b0, b1);
+                            mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
+                        }
+                    }
+                }
                 if (kTma) sm100::fence_proxy_async_smem();  // generic writes above before the next tensor copy
                 __syncwarp();
                 if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
             }
-        }
 
-        // ---- merge the four warps' states; write the output or a partial ----
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        if ((lane & 3) == 0) {
-            stats[(warp * 16 + r0) * 2 + 0] = m0;
-            stats[(warp * 16 + r0) * 2 + 1] = l0;
-            stats[(warp * 16 + r1) * 2 + 0] = m1;
-            stats[(warp * 16 + r1) * 2 + 1] = l1;
-        }
-        if constexpr (kFp8) {
-            // accumulator tile nd, column pair (2c, 2c + 1) holds dims 32c + nd and 32c + 16 + nd
-            float *s0 = scratch + (warp * 16 + r0) * D + 32 * (lane & 3);
-            float *s1 = scratch + (warp * 16 + r1) * D + 32 * (lane & 3);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                *reinterpret_cast<float4 *>(s0 + 4 * i) =
-                    make_float4(acc[4 * i][0], acc[4 * i + 1][0], acc[4 * i + 2][0], acc[4 * i + 3][0]);
-                *reinterpret_cast<float4 *>(s0 + 16 + 4 * i) =
-                    make_float4(acc[4 * i][1], acc[4 * i + 1][1], acc[4 * i + 2][1], acc[4 * i + 3][1]);
-                *reinterpret_cast<float4 *>(s1 + 4 * i) =
-                    make_float4(acc[4 * i][2], acc[4 * i + 1][2], acc[4 * i + 2][2], acc[4 * i + 3][2]);
-                *reinterpret_cast<float4 *>(s1 + 16 + 4 * i) =
-                    make_float4(acc[4 * i][3], acc[4 * i + 1][3], acc[4 * i + 2][3], acc[4 * i + 3][3]);
+            // ---- merge the four warps' states; write the output or a partial ----
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            if ((lane & 3) == 0) {
+                stats[(warp * 16 + r0) * 2 + 0] = m0;
+                stats[(warp * 16 + r0) * 2 + 1] = l0;
+                stats[(warp * 16 + r1) * 2 + 0] = m1;
+                stats[(warp * 16 + r1) * 2 + 1] = l1;
             }
-        } else
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int col = n * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2 *>(scratch + (warp * 16 + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(scratch + (warp * 16 + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
+            for (int n = 0; n < D / 8; ++n) {
+                const int col = n * 8 + 2 * (lane & 3);
+                *reinterpret_cast<float2 *>(scratch + (warp * 16 + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
+                *reinterpret_cast<float2 *>(scratch + (warp * 16 + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
+            }
         }
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(merge_in);
@@ -777,7 +865,7 @@ int num_sms_of_current_device(int *dev_out) {
     return sms[dev];
 }
 
-template <int D, bool kTma, bool kFp8 = false>
+template <int D, bool kTma, bool kFp8 = false, int kNH = 1>
 int launch_decode_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                        cudaStream_t stream) {
     static bool configured[64] = {false};
@@ -785,12 +873,12 @@ int launch_decode_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const Decod
     if (num_sms_of_current_device(&dev) < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
     constexpr int kSmem = DecodeLayout<D, kTma, kFp8>::kSmemBytes;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma, kFp8>,
+        cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma, kFp8, kNH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
         configured[dev] = true;
     }
-    decode_bf16_kernel<D, kTma, kFp8><<<grid, DecodeLayout<D, kTma, kFp8>::kThreads, kSmem, stream>>>(tk, tv, p);
+    decode_bf16_kernel<D, kTma, kFp8, kNH><<<grid, DecodeLayout<D, kTma, kFp8>::kThreads, kSmem, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
     return BSP_OK;
@@ -938,7 +1026,8 @@ int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pa
     int rc = make_tmap(&tk, k_pages, 1, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
     if (rc == BSP_OK) rc = make_tmap(&tv, v_pages, 1, P.head_dim, P.num_kv_heads, rows, 1, p.box_rows);
     if (rc != BSP_OK) return rc;
-    return launch_decode_bf16<128, true, true>(tk, tv, p, grid, stream);
+    return plan->group <= 8 ? launch_decode_bf16<128, true, true, 1>(tk, tv, p, grid, stream)
+                            : launch_decode_bf16<128, true, true, 2>(tk, tv, p, grid, stream);
 }
 
 int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace, cudaStream_t stream) {
