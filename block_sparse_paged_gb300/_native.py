@@ -38,7 +38,8 @@ EXPORTED = ["bsp_default_num_ctas", "bsp_workspace_size", "bsp_host_staging_size
 class Problem(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("window_left", ctypes.c_int32), ("logits_soft_cap", ctypes.c_float)]
+                ("dtype", ctypes.c_int32), ("window_left", ctypes.c_int32), ("logits_soft_cap", ctypes.c_float),
+                ("sink", ctypes.c_void_p)]
 
 
 class Capacity(ctypes.Structure):

@@ -149,10 +149,13 @@ class PagedAttention:
     # ---- run ----------------------------------------------------------------
     def run(self, q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, kv_indices: torch.Tensor,
             sm_scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            stream=None, return_lse: bool = True, k_scale: float = 1.0, v_scale: float = 1.0):
+            stream=None, return_lse: bool = True, k_scale: float = 1.0, v_scale: float = 1.0,
+            sink: torch.Tensor | None = None):
         """Attention of the planned batch. k_pages / v_pages are in the
         problem's dtype, or, for bf16 decode, torch.float8_e4m3fn pools read as
-        k_scale * k_pages and v_scale * v_pages (one scale per pool)."""
+        k_scale * k_pages and v_scale * v_pages (one scale per pool). sink:
+        float32 [H_qo] on the device, one extra softmax logit per query head
+        without a value row (the attention-sink variant), or None."""
         if self.info is None:
             raise RuntimeError("plan() must be called before run()")
         P = self.problem
@@ -180,6 +183,7 @@ class PagedAttention:
         tail = [ctypes.c_float(sm_scale), _dev(out, "out", self.dtype, dev),
                 None if lse is None else _dev(lse, "lse", torch.float32, dev),
                 ctypes.c_void_p(self.workspace.data_ptr())]
+        self._set_sink(sink)
         with torch.cuda.device(dev):
             s = _stream_handle(stream)
             if fp8:
@@ -190,6 +194,15 @@ class PagedAttention:
             else:
                 N.check(self.lib.bsp_prefill_run(*args, k_pages.shape[0], *tail, s))
         return (out, lse) if return_lse else out
+
+    def _set_sink(self, sink):
+        if sink is None:
+            self.info.problem.sink = None
+            return
+        if sink.dim() != 1 or sink.shape[0] != self.problem.num_qo_heads:
+            raise ValueError(f"sink must be [{self.problem.num_qo_heads}]")
+        self.info.problem.sink = _dev(sink, "sink", torch.float32, self.device).value
+        self._sink_ref = sink  # the kernel reads it during the run
 
     def run_stages(self, q, k_pages, v_pages, kv_indices, sm_scale, out, lse, stream=None, events=None):
         """The run as its launches on `stream`: the attention kernel, then for
@@ -203,6 +216,7 @@ class PagedAttention:
             ws = ctypes.c_void_p(self.workspace.data_ptr())
             o_p = _dev(out, "out", self.dtype, dev)
             l_p = None if lse is None else _dev(lse, "lse", torch.float32, dev)
+            self._set_sink(None)
             if events:
                 events[0].record(st)
             N.check(self.lib.bsp_run_attention(ctypes.byref(self.info), _dev(q, "q", self.dtype, dev),

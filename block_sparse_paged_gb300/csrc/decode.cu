@@ -128,6 +128,7 @@ struct DecodeParams {
     int soft_cap_on;         // scores: tanh(s * cap_in) * cap_out instead of s * scale_log2
     float cap_in, cap_out;   // sm_scale / c and c * log2(e)
     float v_scale;           // output factor (per-tensor V scale of an e4m3 pool; else 1)
+    const float *sink;       // per-qo-head sink logits, or null
 };
 
 // Merge of one reduction-map entry by warps w = 0..nwarps-1 of the CTA that
@@ -166,12 +167,14 @@ __device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_mer
                 }
             }
         }
-        const float inv = M != -INFINITY ? 1.f / L : 0.f;
+        float inv = M != -INFINITY ? 1.f / L : 0.f;
+        float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
+        if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
         const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
         OutT *dst = static_cast<OutT *>(p.o) + orow * D + lane * E;
 #pragma unroll
         for (int i = 0; i < E; ++i) dst[i] = from_float<OutT>(acc[i] * inv);
-        if (lane == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
+        if (lane == 0 && p.lse) p.lse[orow] = lse_row;
     }
 }
 
@@ -692,6 +695,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             }
             if (w.slot < 0) {
                 const size_t orow = (size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g + row;
+                if (p.sink) val *= fold_sink(lse_v, p.sink[w.kv_head * g + row]);
                 static_cast<__nv_bfloat16 *>(p.o)[orow * D + d] = __float2bfloat16_rn(val);
                 if (d == 0 && p.lse) p.lse[orow] = lse_v;
             } else {
@@ -768,9 +772,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
                 m = mn;
             }
             const bool empty = !(l > 0.f);  // no visible key (empty chunk, or all before the window)
-            const float inv = empty ? 0.f : 1.f / l;
-            const float lse_v = empty ? -INFINITY : (m + log2f(l)) * kLn2;
+            float inv = empty ? 0.f : 1.f / l;
+            float lse_v = empty ? -INFINITY : (m + log2f(l)) * kLn2;
             if (w.slot < 0) {
+                if (p.sink) inv *= fold_sink(lse_v, p.sink[w.kv_head * p.g + row]);
                 float *o = static_cast<float *>(p.o) + qrow * D;
 #pragma unroll
                 for (int i = 0; i < E; ++i) o[lane + 32 * i] = acc[i] * inv;
@@ -807,6 +812,7 @@ struct ReduceParams {
     void *o;
     float *lse;
     int H_qo, g, tile_rows;
+    const float *sink;  // per-qo-head sink logits, or null
 };
 
 template <int D, typename OutT>
@@ -843,12 +849,14 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
                 for (int i = 0; i < E; ++i) acc[i] = fmaf(wgt, po[prow * D + lane * E + i], acc[i]);
             }
         }
-        const float inv = M != -INFINITY ? 1.f / L : 0.f;
+        float inv = M != -INFINITY ? 1.f / L : 0.f;
+        float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
+        if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
         const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
         OutT *o = static_cast<OutT *>(p.o) + orow * D + lane * E;
 #pragma unroll
         for (int i = 0; i < E; ++i) o[i] = from_float<OutT>(acc[i] * inv);
-        if (lane == 0 && p.lse) p.lse[orow] = M != -INFINITY ? M + logf(L) : -INFINITY;
+        if (lane == 0 && p.lse) p.lse[orow] = lse_row;
     }
 }
 
@@ -940,6 +948,7 @@ int decode_params(const bsp_plan_info *plan, const void *q, const void *k_pages,
     const float qk_scale = sm_scale * k_scale;
     p.scale_log2 = qk_scale * kLog2e;
     p.v_scale = v_scale;
+    p.sink = P.sink;
     p.window_left = P.window_left;
     p.soft_cap_on = P.logits_soft_cap > 0.f;
     p.cap_in = p.soft_cap_on ? qk_scale / P.logits_soft_cap : 0.f;
@@ -1043,6 +1052,7 @@ int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspac
     p.H_qo = P.num_qo_heads;
     p.g = plan->group;
     p.tile_rows = plan->tile_rows;
+    p.sink = P.sink;
     const bool bf = P.dtype == BSP_DTYPE_BF16;
     switch (P.head_dim) {
         case 32: return bf ? launch_reduce_t<32, __nv_bfloat16>(p, stream) : launch_reduce_t<32, float>(p, stream);

@@ -74,6 +74,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Attention sink (FlashInfer 原理 overview, ⑧, the AttentionSink variant): the
+// per-head logit sk joins the softmax normaliser without a value row, which is
+// the state (O, lse) merged with (0, sk). Returns the factor on O; lse becomes
+// the merged LSE (natural log). An empty state becomes (0, sk).
+__device__ __forceinline__ float fold_sink(float &lse, float sk) {
+    if (sk == -INFINITY) return 1.f;
+    if (lse == -INFINITY) {
+        lse = sk;
+        return 0.f;
+    }
+    const float mx = fmaxf(lse, sk);
+    const float ea = expf(lse - mx), eb = expf(sk - mx);
+    lse = mx + logf(ea + eb);
+    return ea / (ea + eb);
+}
+
 // (lo, hi) -> f16x2, finite values saturated to +-65504 (lo in the low half)
 __device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
     uint32_t r;

@@ -100,6 +100,7 @@ struct PrefillParams {
     int window_left;         // > 0: key j is masked for a row at position i if j < i + kv_len - qo_len - window_left
     int soft_cap_on;         // scores become tanh(s * cap_in); scale_log2 is then c * log2(e)
     float cap_in;            // sm_scale / c
+    const float *sink;       // per-qo-head sink logits, or null (applied to finished rows)
 };
 
 struct Ctx {
@@ -528,11 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kD; ++i) ov[i] = 0.f;
             }
             const bool has = l > 0.f;
-            const float inv = has ? 1.f / l : 0.f;
-            const float lse_v = has ? (m + log2f(l)) * dev::kLn2 : -INFINITY;
+            float inv = has ? 1.f / l : 0.f;
+            float lse_v = has ? (m + log2f(l)) * dev::kLn2 : -INFINITY;
             const size_t orow = (size_t)(w.q_tok0 + rt / g) * p.H_qo + (size_t)w.kv_head * g + (rt % g);
             const size_t prow = (size_t)w.slot * p.tile_rows + rt;
             const int n_rows = w.n_pos * g;  // real rows of the tile
+            if (p.sink && w.slot < 0 && rt < n_rows) inv *= dev::fold_sink(lse_v, p.sink[w.kv_head * g + rt % g]);
             if (w.slot < 0) {
                 // bf16 output through this warp's swizzled staging, 64 columns at a
                 // time: each thread writes its row, then every store instruction
@@ -636,6 +638,7 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.window_left = P.window_left;
     p.soft_cap_on = P.logits_soft_cap > 0.f;
     p.cap_in = p.soft_cap_on ? sm_scale / P.logits_soft_cap : 0.f;
+    p.sink = P.sink;
     if (p.soft_cap_on) p.scale_log2 = P.logits_soft_cap * dev::kLog2e;
     p.H_qo = P.num_qo_heads;
     p.g = g;

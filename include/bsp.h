@@ -99,6 +99,14 @@ typedef struct bsp_problem {
     float logits_soft_cap; /* c > 0: scores s become c * tanh(s / c) (s already
                               scaled by sm_scale) before masking and softmax;
                               0: none                                            */
+    /* Attention sink (FlashInfer 原理 overview, ⑧, the AttentionSink variant):
+     * device, float [H_qo], one logit per query head that joins every row's
+     * softmax normaliser without a value row:
+     *     LSE = log(exp(sink[h]) + sum_j exp(s_j)),  O = sum_j exp(s_j - LSE) v_j
+     * (a row with no visible key: O = 0, LSE = sink[h]). NULL: none. Read at
+     * run time from the plan's copy of the problem, so a plan shared by layers
+     * may point it at each layer's sinks between runs. Not owned.              */
+    const float *sink;
 } bsp_problem;
 
 /* Upper bounds fixed when the workspace is sized (technical review §6.4:

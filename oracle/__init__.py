@@ -57,7 +57,7 @@ class COracle:
     def __init__(self, path: str):
         lib = ctypes.CDLL(path)
         i32, i64, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
-        lib.oracle_attention_rows.argtypes = [i32, i32, i32, i32, i32, i32, f64, i32, f64,
+        lib.oracle_attention_rows.argtypes = [i32, i32, i32, i32, i32, i32, f64, i32, f64, vp,
                                               vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, i32]
         lib.oracle_attention_rows.restype = ctypes.c_int
         lib.oracle_merge_states.argtypes = [i64, i32, vp, vp, vp, vp, vp, vp]
@@ -79,8 +79,9 @@ class COracle:
     def attention_rows(self, q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, last_page_len,
                        num_qo_heads: int, num_kv_heads: int, page_size: int, causal: bool,
                        sm_scale: float, sel_token, sel_head, num_threads: int = 0,
-                       window_left: int = -1, soft_cap: float = 0.0):
+                       window_left: int = -1, soft_cap: float = 0.0, sink=None):
         """(O [n, D], LSE [n]) in fp64 for the selected (token, head) pairs.
+        sink: None or one logit per query head (the attention-sink variant).
 
         q: [n_tokens, H_qo, D]; k_pages, v_pages: [num_pages, page_size, H_kv, D],
         any float dtype (converted to float32, which holds bf16 and fp32 exactly).
@@ -94,9 +95,14 @@ class COracle:
         n = st.shape[0]
         o = np.zeros((n, D), np.float64)
         lse = np.zeros((n,), np.float64)
+        sk = None
+        if sink is not None:
+            sk = _c(sink, np.float64)
+            if sk.shape != (num_qo_heads,):
+                raise ValueError("sink must hold one value per query head")
         rc = self.lib.oracle_attention_rows(len(qi) - 1, num_qo_heads, num_kv_heads, D, page_size,
                                             int(bool(causal)), float(sm_scale), int(window_left), float(soft_cap),
-                                            _ptr(qi), _ptr(ki), _ptr(kx), _ptr(lp),
+                                            None if sk is None else _ptr(sk), _ptr(qi), _ptr(ki), _ptr(kx), _ptr(lp),
                                             _ptr(q), _ptr(k), _ptr(v), n, _ptr(st), _ptr(sh),
                                             _ptr(o), _ptr(lse), int(num_threads))
         if rc != 0:
@@ -105,14 +111,15 @@ class COracle:
 
     def attention(self, q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, last_page_len,
                   num_qo_heads: int, num_kv_heads: int, page_size: int, causal: bool,
-                  sm_scale: float, num_threads: int = 0, window_left: int = -1, soft_cap: float = 0.0):
+                  sm_scale: float, num_threads: int = 0, window_left: int = -1, soft_cap: float = 0.0,
+                  sink=None):
         """All outputs: O [n_tokens, H_qo, D] and LSE [n_tokens, H_qo], fp64."""
         n_tok = int(np.asarray(qo_indptr)[-1])
         tok = np.repeat(np.arange(n_tok, dtype=np.int64), num_qo_heads)
         head = np.tile(np.arange(num_qo_heads, dtype=np.int32), n_tok)
         o, lse = self.attention_rows(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices,
                                      last_page_len, num_qo_heads, num_kv_heads, page_size, causal,
-                                     sm_scale, tok, head, num_threads, window_left, soft_cap)
+                                     sm_scale, tok, head, num_threads, window_left, soft_cap, sink)
         D = o.shape[-1]
         return o.reshape(n_tok, num_qo_heads, D), lse.reshape(n_tok, num_qo_heads)
 

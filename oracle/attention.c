@@ -30,11 +30,17 @@
  *   - logits soft-cap (FlashInfer: Making Attention Fit the Serving Workload,
  *     eq 8): with c = soft_cap > 0 each allowed score becomes c * tanh(s / c),
  *     s being the scaled score, before the softmax;
+ *   - attention sink (FlashInfer 原理 overview, ⑧, the AttentionSink variant:
+ *     a per-head value enters the online softmax's (m, d) as one more logit
+ *     and the output is normalised by that larger d): with sink != NULL,
+ *     LSE = log(exp(sink[h]) + sum_j exp(s_j)) and O = sum_j exp(s_j - LSE) v_j;
+ *     the sink has no value row, so a row with no visible key gets O = 0,
+ *     LSE = sink[h];
  *   - stable merge with the empty-state rule (FlashInfer: Making Attention Fit
  *     the Serving Workload, §3.2 eq 6 and §3.3 Algorithm 1).
  *
  * Inputs are float (bf16 and fp32 values are exact in float); all arithmetic
- * is double. An empty key set gives O = 0, LSE = -inf.
+ * is double. An empty key set gives O = 0, LSE = -inf (without a sink).
  */
 #include <math.h>
 #include <stddef.h>
@@ -90,7 +96,7 @@ static int32_t request_of_token(const int32_t *qo_indptr, int32_t batch, int64_t
  */
 int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
                           int32_t page_size, int32_t causal, double sm_scale,
-                          int32_t window_left, double soft_cap,
+                          int32_t window_left, double soft_cap, const double *sink,
                           const int32_t *qo_indptr, const int32_t *kv_indptr,
                           const int32_t *kv_indices, const int32_t *last_page_len,
                           const float *q, const float *k_pages, const float *v_pages,
@@ -129,7 +135,7 @@ int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
             if (j0 < 0) j0 = 0;
         }
         for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
-        if (n_vis <= j0) { lse_out[s] = -INFINITY; continue; }
+        if (n_vis <= j0) { lse_out[s] = sink ? sink[h] : -INFINITY; continue; }
 
         const float *qv = q + (tok * H_qo + h) * (int64_t)D;
         double *sc = (double *)malloc(sizeof(double) * (size_t)n_vis);
@@ -146,8 +152,10 @@ int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
         /* LSE = m + log sum exp(s_j - m) */
         double m = sc[j0];
         for (int64_t j = j0 + 1; j < n_vis; ++j) if (sc[j] > m) m = sc[j];
+        if (sink && sink[h] > m) m = sink[h];
         double z = 0.0;
         for (int64_t j = j0; j < n_vis; ++j) z += exp(sc[j] - m);
+        if (sink) z += exp(sink[h] - m);                         /* the sink logit, no value row */
         const double lse = m + log(z);
         /* O = sum_j exp(s_j - LSE) v_j */
         for (int64_t j = j0; j < n_vis; ++j) {

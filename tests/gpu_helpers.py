@@ -25,7 +25,7 @@ def to_dev(batch, dev="cuda"):
             torch.from_numpy(np.ascontiguousarray(batch.kv_indices, np.int32)).to(dev))
 
 
-def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=None, max_qo=None):
+def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=None, max_qo=None, sink=None):
     """Plan + run through the library; returns (O, LSE) on the host and the runner."""
     mode = mode or ("decode" if batch.is_decode else "prefill")
     pa = bsp.PagedAttention(mode, batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
@@ -35,7 +35,8 @@ def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=
     qo = None if mode == "decode" and batch.is_decode else batch.qo_indptr
     pa.plan(batch.kv_indptr, batch.last_page_len, qo_indptr=qo)
     q, k, v, idx = dev_tensors or to_dev(batch)
-    out, lse = pa.run(q, k, v, idx, batch.sm_scale)
+    sk = None if sink is None else torch.as_tensor(np.asarray(sink, np.float32)).to(q.device)
+    out, lse = pa.run(q, k, v, idx, batch.sm_scale, sink=sk)
     torch.cuda.synchronize()
     return out, lse, pa
 
@@ -76,8 +77,8 @@ def compare(out, lse, O_ref, L_ref, dtype, rows=None, rounding_aware=False):
     return err_o, err_l
 
 
-def oracle_full(batch, num_threads=0):
-    return oracle.attention_of(batch, num_threads=num_threads)
+def oracle_full(batch, num_threads=0, sink=None):
+    return oracle.attention_of(batch, num_threads=num_threads, sink=sink)
 
 
 def sample_rows(batch, n, seed):

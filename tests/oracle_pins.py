@@ -253,6 +253,69 @@ def pin_soft_cap_one_key(orc):
         assert np.allclose(o[0, 0], v[0, 0, 0], rtol=0, atol=1e-15)
 
 
+def pin_sink_one_key(orc):
+    """Attention sink (overview ⑧, the AttentionSink variant: the sink joins the
+    softmax's (m, d) as one more logit, the output is normalised by that d) with
+    one key and two query heads on one kv head, each with its own sink: closed
+    form O_h = v e^{s_h} / (e^{s_h} + e^{sink_h}), LSE_h = log(e^{s_h} + e^{sink_h})."""
+    rng = np.random.default_rng(37)
+    D = 8
+    q = rng.standard_normal((1, 2, D)).astype(np.float32)
+    k = rng.standard_normal((1, 1, 1, D)).astype(np.float32)
+    v = rng.standard_normal((1, 1, 1, D)).astype(np.float32)
+    sink = np.array([0.3, -1.7])
+    o, lse = orc.attention(q, k, v, [0, 1], [0, 1], [0], [1], 2, 1, 1, False, 0.6, sink=sink)
+    for h in range(2):
+        s = 0.6 * float(np.dot(q[0, h].astype(np.float64), k[0, 0, 0].astype(np.float64)))
+        assert abs(lse[0, h] - math.log(math.exp(s) + math.exp(sink[h]))) < 1e-12
+        w = math.exp(s) / (math.exp(s) + math.exp(sink[h]))
+        assert np.allclose(o[0, h], w * v[0, 0, 0].astype(np.float64), rtol=0, atol=1e-14)
+
+
+def pin_sink_virtual_key(orc):
+    """A sink equals one extra key with a zero value row whose score is the sink
+    (the sink is a logit without a value): every query gets q[0] = 1 and the extra
+    key, placed first, k = (sink / sm_scale, 0, ...), so its score is exactly the
+    sink; placing it first keeps the other keys' bottom-right causal visibility."""
+    rng = np.random.default_rng(41)
+    D, H, sm = 8, 3, 0.5
+    sink = np.array([1.5, -0.75, 3.0])
+    for causal in (False, True):
+        qo, kv = [1, 4, 3], [5, 4, 7]
+        n_tok = sum(qo)
+        q = rng.standard_normal((n_tok, H, D)).astype(np.float32)
+        q[:, :, 0] = 1.0
+        ks = [rng.standard_normal((n, H, D)).astype(np.float32) for n in kv]
+        vs = [rng.standard_normal((n, H, D)).astype(np.float32) for n in kv]
+        virt_k = np.zeros((1, H, D), np.float32)
+        virt_k[0, :, 0] = sink / sm
+        virt_v = np.zeros((1, H, D), np.float32)
+
+        def batch(extra):
+            kp = np.concatenate([np.concatenate(([virt_k] if extra else []) + [k]) for k in ks])
+            vp = np.concatenate([np.concatenate(([virt_v] if extra else []) + [v]) for v in vs])
+            lens = [n + int(extra) for n in kv]
+            return (q, kp.reshape(-1, 1, H, D), vp.reshape(-1, 1, H, D), np.cumsum([0] + qo),
+                    np.cumsum([0] + lens), np.arange(sum(lens)), np.ones(len(kv), np.int32), H, H, 1, causal, sm)
+        O1, L1 = orc.attention(*batch(False), sink=sink)
+        O2, L2 = orc.attention(*batch(True))
+        assert np.allclose(L1, L2, rtol=0, atol=1e-12) and np.allclose(O1, O2, rtol=0, atol=1e-12), causal
+
+
+def pin_sink_limits(orc):
+    """A sink of -inf is no sink (bit-identical); a row with no visible key keeps
+    O = 0 and gets LSE = sink (the normaliser holds only the sink)."""
+    batch = workloads.paged_batch(43, [1, 2, 1], [6, 0, 3], 4, 2, 8, 2, "f32", causal=False)
+    args = (batch.q.float().numpy(), batch.k_pages.float().numpy(), batch.v_pages.float().numpy(),
+            batch.qo_indptr, batch.kv_indptr, batch.kv_indices, batch.last_page_len, 4, 2, 2, False, 0.35)
+    O0, L0 = orc.attention(*args)
+    On, Ln = orc.attention(*args, sink=np.full(4, -np.inf))
+    assert np.array_equal(O0, On) and np.array_equal(L0, Ln)
+    sink = np.array([0.5, -2.0, 1.25, 7.0])
+    Os, Ls = orc.attention(*args, sink=sink)
+    assert np.all(Os[1:3] == 0) and np.array_equal(Ls[1:3], np.tile(sink, (2, 1)))
+
+
 def pin_variants_library(orc):
     """Sliding window and soft-cap on contiguous batches vs library routines on
     the explicitly masked, explicitly capped dense scores."""
@@ -361,4 +424,5 @@ def pin_poison_unread(orc):
 ALL_PINS = [pin_merge_worked_example, pin_merge_masses, pin_online_two_tiles, pin_one_key,
             pin_page_mapping, pin_toy_bsr, pin_toy_bsr_attention, pin_bsr_page_table, pin_dense_library,
             pin_permuted_equals_contiguous, pin_causal_prefix, pin_empty, pin_merge_algebra,
-            pin_poison_unread, pin_soft_cap_one_key, pin_variants_library]
+            pin_poison_unread, pin_soft_cap_one_key, pin_variants_library, pin_sink_one_key,
+            pin_sink_virtual_key, pin_sink_limits]

@@ -17,7 +17,7 @@ def bsp():
     return lib()
 
 
-def run_fp8(bsp, b, f8, num_ctas=None, repeats=1):
+def run_fp8(bsp, b, f8, num_ctas=None, repeats=1, sink=None):
     pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
                             torch.bfloat16, max_batch=b.batch, num_ctas=num_ctas, window_left=b.window_left,
                             logits_soft_cap=b.soft_cap)
@@ -26,8 +26,9 @@ def run_fp8(bsp, b, f8, num_ctas=None, repeats=1):
     k = f8.k8.cuda().view(torch.float8_e4m3fn)
     v = f8.v8.cuda().view(torch.float8_e4m3fn)
     idx = torch.from_numpy(np.ascontiguousarray(b.kv_indices, np.int32)).cuda()
+    sk = None if sink is None else torch.tensor(sink, dtype=torch.float32, device="cuda")
     for _ in range(repeats):
-        out, lse = pa.run(q, k, v, idx, b.sm_scale, k_scale=f8.k_scale, v_scale=f8.v_scale)
+        out, lse = pa.run(q, k, v, idx, b.sm_scale, k_scale=f8.k_scale, v_scale=f8.v_scale, sink=sk)
     torch.cuda.synchronize()
     return out, lse, pa
 
@@ -59,6 +60,17 @@ def test_fp8_decode(bsp, case):
     out, lse, pa = run_fp8(bsp, b, f8, num_ctas=C)
     compare(out, lse, O, L, "bf16")
     assert pa.check_device_error() == 0
+
+
+def test_fp8_sink(bsp):
+    """Attention sink on the e4m3 path: split outputs (fused merge) and an empty request."""
+    b = workloads.paged_batch(112, [1] * 4, [3000, 0, 700, 4100], 32, 8, 128, 16, "bf16", extra_pages=1)
+    f8 = workloads.fp8_kv(b)
+    sk = np.random.default_rng(112).uniform(-2.0, 4.0, size=32)
+    kd, vd = oracle_kv(f8)
+    O, L = oracle.attention_of(b, k=kd, v=vd, sink=sk)
+    out, lse, _ = run_fp8(bsp, b, f8, num_ctas=19, sink=sk)
+    compare(out, lse, O, L, "bf16")
 
 
 def test_fp8_scales_are_applied(bsp):

@@ -1,6 +1,8 @@
 """Attention variants (FlashInfer 原理 overview, ⑧; FlashInfer: Making Attention
-Fit the Serving Workload, eq 8): sliding window and logits soft-cap, on the
-decode and prefill paths, against the oracle on the same seeded inputs."""
+Fit the Serving Workload, eq 8): sliding window, logits soft-cap and attention
+sink, on the decode and prefill paths, against the oracle on the same seeded
+inputs."""
+import numpy as np
 import pytest
 
 import oracle
@@ -67,3 +69,49 @@ def test_prefill_window_full_size(bsp):
     tok, head = sample_rows(b, 256, 25)
     O, L = oracle.attention_rows_of(b, tok, head)
     compare(out, lse, O, L, "bf16", rows=(tok, head))
+
+
+def sinks(h, seed):
+    """Per-head sink logits around the scale of the scores, one of them -inf."""
+    x = np.random.default_rng(seed).uniform(-2.0, 4.0, size=h)
+    x[h // 2] = -np.inf
+    return x
+
+
+SINK_DECODE = [
+    # (seed, kv lens, H_qo, H_kv, D, page, dtype, num_ctas): splits, an empty request
+    (121, [3000, 0, 900, 4100, 1, 250], 32, 8, 128, 16, "bf16", 29),
+    (122, [700, 5, 0, 1200], 16, 4, 64, 4, "f32", 9),
+    (123, [2000, 64, 0, 1500], 64, 8, 128, 1, "bf16", 11),
+]
+
+
+@pytest.mark.parametrize("case", SINK_DECODE, ids=[f"sink_decode{c[0]}" for c in SINK_DECODE])
+def test_decode_sink(bsp, case):
+    seed, kv, hq, hk, D, ps, dt, C = case
+    b = workloads.paged_batch(seed, [1] * len(kv), kv, hq, hk, D, ps, dt, extra_pages=2)
+    sk = sinks(hq, seed)
+    O, L = oracle_full(b, sink=sk)
+    out, lse, pa = run_batch(bsp, b, num_ctas=C, sink=sk)
+    compare(out, lse, O, L, dt)
+    assert pa.check_device_error() == 0
+
+
+SINK_PREFILL = [
+    # (seed, qo lens, kv lens, H_qo, H_kv, page, causal, window, num_ctas): split rows go
+    # through the merge kernel, whole rows through the epilogue
+    (124, [300, 65, 1000], [300, 65, 1000], 32, 8, 16, True, -1, 13),
+    (125, [200, 90], [700, 90], 16, 4, 1, True, 77, 7),
+    (126, [128, 300], [128, 500], 32, 8, 32, False, -1, 40),
+]
+
+
+@pytest.mark.parametrize("case", SINK_PREFILL, ids=[f"sink_prefill{c[0]}" for c in SINK_PREFILL])
+def test_prefill_sink(bsp, case):
+    seed, qo, kv, hq, hk, ps, causal, w, C = case
+    b = with_variant(workloads.paged_batch(seed, qo, kv, hq, hk, 128, ps, "bf16", causal=causal, extra_pages=2), w)
+    sk = sinks(hq, seed)
+    O, L = oracle_full(b, sink=sk)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=C, sink=sk)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0

@@ -37,6 +37,9 @@ MUTATIONS = [
     ("soft_cap_scale_dropped", "sc[j] = soft_cap * tanh(sc[j] / soft_cap);", "sc[j] = tanh(sc[j]);"),
     ("window_off_by_one", "j0 = i + kv_len - qo_len - window_left;", "j0 = i + kv_len - qo_len - window_left + 1;"),
     ("merge_naive_average", "o[d] = (a * oa[d] + bb * ob[d]) / (a + bb);", "o[d] = 0.5 * (oa[d] + ob[d]);"),
+    ("sink_left_out_of_normaliser", "if (sink) z += exp(sink[h] - m);", "if (sink) z += 0.0;"),
+    ("sink_of_kv_head", "if (sink) z += exp(sink[h] - m);", "if (sink) z += exp(sink[hk] - m);"),
+    ("sink_empty_row_stays_empty", "lse_out[s] = sink ? sink[h] : -INFINITY;", "lse_out[s] = -INFINITY;"),
 ]
 
 
