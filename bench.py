@@ -431,27 +431,7 @@ def secondary(bsp, dev, args, pk):
     r["workload"] = "32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16"
     res["vector_sparse_decode"] = r
     del perm, cont
-    # ragged causal prefill
-    b = workloads.ragged_causal_prefill_bf16()
-    try:
-        pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
-                                torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
-        attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
-        fl = prefill_flops(b)
-        tf = fl / ((attn + merge) * 1e-3) / 1e12
-        ka = fl / (attn * 1e-3) / 1e12
-        res["ragged_causal_prefill"] = {
-            "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "flops": fl,
-            "attn_ms": round(attn, 4), "merge_ms": round(merge, 4),
-            "workload": "16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, D 128, bf16, causal",
-            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(ka, 1),
-                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ka / pk["bf16_tflops"], 4),
-                         "peak_source": "measured (cuBLAS bf16 burst; the kernel is timed alone)",
-                         "traffic": profile_traffic("prefill_ragged_causal", kernel_digest(*PREFILL_SOURCES)),
-                         "algorithmic_flops_per_launch": fl}}
-    except Exception as e:  # the prefill kernel may not be built for this shape
-        res["ragged_causal_prefill"] = {"unavailable": str(e)[:200]}
-    del b
+    res["ragged_causal_prefill"] = ragged_prefill(bsp, dev, steps, warm, pk)
     torch.cuda.empty_cache()
     res["vector_sparse_prefill"] = vector_sparse_prefill(bsp, dev, max(3, steps // 10), warm, pk)
     b = workloads.bsr_prefill_bf16()
@@ -470,6 +450,27 @@ def secondary(bsp, dev, args, pk):
     return res
 
 
+def ragged_prefill(bsp, dev, steps, warm, pk):
+    """The ragged causal prefill workload, kernel-only timing with a roofline."""
+    import workloads
+    b = workloads.ragged_causal_prefill_bf16()
+    pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
+                            torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+    attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
+    fl = prefill_flops(b)
+    tf = fl / ((attn + merge) * 1e-3) / 1e12
+    ka = fl / (attn * 1e-3) / 1e12
+    return {
+        "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "flops": fl,
+        "attn_ms": round(attn, 4), "merge_ms": round(merge, 4),
+        "workload": "16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, D 128, bf16, causal",
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(ka, 1),
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ka / pk["bf16_tflops"], 4),
+                     "peak_source": "measured (cuBLAS bf16 burst; the kernel is timed alone)",
+                     "traffic": profile_traffic("prefill_ragged_causal", kernel_digest(*PREFILL_SOURCES)),
+                     "algorithmic_flops_per_launch": fl}}
+
+
 def fp8_decode(bsp, dev, steps, warm, pk):
     """The batched decode workload with e4m3 K / V pools (one scale each):
     algorithmic bytes as for bf16 but one byte per K / V element."""
@@ -485,28 +486,44 @@ def fp8_decode(bsp, dev, steps, warm, pk):
     idx = torch.from_numpy(np.ascontiguousarray(b.kv_indices, np.int32)).to(dev)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
 
     def run():
-        pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, k_scale=f8.k_scale, v_scale=f8.v_scale)
-    for _ in range(warm):
-        run()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, k_scale=f8.k_scale, v_scale=f8.v_scale, stream=st)
+    # 10 launches per CUDA graph replay: the host's per-call cost stays out of the kernel time
+    reps = 10
+    with torch.cuda.stream(st):
+        for _ in range(warm):
+            run()
     torch.cuda.synchronize()
-    ev[0].record()
-    for i in range(steps):
-        run()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for _ in range(reps):
+            run()
+    graph.replay()
+    n_rep = max(1, steps // reps)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()  # replay() launches on the current stream
+    for i in range(n_rep):
+        graph.replay()
         ev[i + 1].record()
     torch.cuda.synchronize()
-    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(n_rep)) / reps
     kv_tokens = int(b.kv_lens.sum())
     nbytes = decode_bytes(b) - kv_tokens * b.num_kv_heads * b.head_dim * 2 * (esize(b) - 1)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    del pa, q, k, v
+    del graph, pa, q, k, v
     torch.cuda.empty_cache()
     return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
             "bytes": nbytes, "tokens_per_s": round(b.batch / (ms * 1e-3), 1),
             "workload": "batched decode (64 requests, KV ~ U{512..8192}, page 16 permuted, 32/8 heads, D 128), "
-                        "K / V e4m3 with one scale per pool, q / o bf16; one launch per step"}
+                        "K / V e4m3 with one scale per pool, q / o bf16; one launch per step, 10 per graph replay",
+            "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel<128, TMA gather, e4m3>",
+                         "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": "measured (STREAM-style copy)",
+                         "traffic": profile_traffic("decode_fp8_batched", kernel_digest(*DECODE_SOURCES)),
+                         "algorithmic_bytes_per_launch": nbytes}}
 
 
 def vector_sparse_prefill(bsp, dev, steps, warm, pk):
@@ -653,7 +670,18 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["ragged_causal_prefill", "fp8_kv_decode"], default=None,
+                    help="run one secondary workload alone (steps / warmup as given) and print its line; "
+                         "for profiling")
     args = ap.parse_args(argv)
+    if args.case:
+        from block_sparse_paged_gb300 import build
+        build.build()
+        import block_sparse_paged_gb300 as bsp
+        dev = torch.device("cuda", 0)
+        fn = {"ragged_causal_prefill": ragged_prefill, "fp8_kv_decode": fp8_decode}[args.case]
+        print(json.dumps({args.case: fn(bsp, dev, args.steps, args.warmup, peaks()[0])}), flush=True)
+        return
     rank, world, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
