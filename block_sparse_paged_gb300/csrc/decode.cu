@@ -55,12 +55,13 @@ constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per
 constexpr int kStages = 5;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 
-// Two e4m3 values (the low and high byte of the low 16 bits of x) to f16x2,
-// the low byte in the low half. Exact: every e4m3 value is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-    uint32_t r;
-    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}\n" : "=r"(r) : "r"(x));
-    return r;
+// Four e4m3 values (the bytes of x, lowest first) to two f16x2: lo = bytes 0
+// and 1, hi = bytes 2 and 3, the lower byte in the lower half. Exact: every
+// e4m3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 // Transpose of an 8 x 8 matrix of 16-bit values held as one register per lane
@@ -427,7 +428,11 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 for (int i = 0; i < 4; ++i) {
                     const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = warp * 16 + rr;
                     vw[i] = sm100::ld_shared_v4(vb + R * 128 + ((qn ^ (R & 7)) << 4));
-                    if (rr >= valid) vw[i] = make_uint4(0, 0, 0, 0);
+                }
+                if (valid < 16) {  // the chunk ends inside this warp's rows (warp-uniform)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (2 * c + (i & 1) + 8 * (i >> 1) >= valid) vw[i] = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
                 if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
@@ -443,8 +448,9 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                     const int h = kk >> 2, j = kk & 3;
                     const uint32_t w0 = j == 0 ? kw[0][h].x : j == 1 ? kw[0][h].y : j == 2 ? kw[0][h].z : kw[0][h].w;
                     const uint32_t w1 = j == 0 ? kw[1][h].x : j == 1 ? kw[1][h].y : j == 2 ? kw[1][h].z : kw[1][h].w;
-                    const uint32_t a[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
-                                           e4m3x2_to_f16x2(w1 >> 16)};
+                    uint32_t a[4];  // rows r, r + 8 x dims {0, 1}, then {2, 3}
+                    e4m3x4_to_f16x4(w0, a[0], a[2]);
+                    e4m3x4_to_f16x4(w1, a[1], a[3]);
 #pragma unroll
                     for (int nh = 0; nh < kNH; ++nh) mma_f16_16816(st[nh][kk & 1], a, qf[kk][nh][0], qf[kk][nh][1]);
                 }
@@ -495,10 +501,11 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                     const uint32_t vd = m == 0 ? vw[3].x : m == 1 ? vw[3].y : m == 2 ? vw[3].z : vw[3].w;
                     const uint32_t lo01 = prmt(va, vb2, 0x5140), lo23 = prmt(va, vb2, 0x7362);
                     const uint32_t hi01 = prmt(vc, vd, 0x5140), hi23 = prmt(vc, vd, 0x7362);
-                    const uint32_t a_e[4] = {e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01),
-                                             e4m3x2_to_f16x2(hi01 >> 16)};
-                    const uint32_t a_o[4] = {e4m3x2_to_f16x2(lo23), e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23),
-                                             e4m3x2_to_f16x2(hi23 >> 16)};
+                    uint32_t a_e[4], a_o[4];
+                    e4m3x4_to_f16x4(lo01, a_e[0], a_e[1]);
+                    e4m3x4_to_f16x4(hi01, a_e[2], a_e[3]);
+                    e4m3x4_to_f16x4(lo23, a_o[0], a_o[1]);
+                    e4m3x4_to_f16x4(hi23, a_o[2], a_o[3]);
 #pragma unroll
                     for (int nh = 0; nh < kNH; ++nh) {
                         mma_f16_16816(oacc[2 * m][nh], a_e, pb[nh][0], pb[nh][1]);

@@ -71,9 +71,11 @@ constexpr int kOffV = kOffK + kKStages * kTile;   // kVStages tiles
 constexpr int kStgWarp = 32 * 128;                 // per softmax warp: 32 rows x 64 bf16, swizzled
 constexpr int kOffStg = kOffV + kVStages * kTile;  // output staging, 8 warps
 constexpr int kOffBar = kOffStg + 8 * kStgWarp;
+// Ring barriers are indexed kKFull0 + stage etc.: one slot per stage of each ring.
 enum Bar {
-    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-    kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
+    kQFull = 0, kQEmpty,
+    kKFull0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages, kVEmpty0 = kVFull0 + kVStages,
+    kSFull0 = kVEmpty0 + kVStages, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree0, kOFree1, kNumBars
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool softmax_arrivals = i == kPFull0 || i == kPFull1 || i == kOFree0 || i == kOFree1;
-            const bool kv_full = i == kKFull0 || i == kKFull1 || i == kVFull0 || i == kVFull1;
+            const bool kv_full = (i >= kKFull0 && i < kKFull0 + kKStages) || (i >= kVFull0 && i < kVFull0 + kVStages);
             mbar_init(bar(i), softmax_arrivals ? 128 : (kv_full && !kTma) ? 32 : 1);  // cp.async: one per lane
         }
         *ctx.abort_flag = 0;
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < nt; ++t, ++j) {
                 const int tok0 = w.kv_start + t * kKvTile;
                 const int valid = min(kKvTile, len - t * kKvTile);
-                const int stage = j & 1, round = j >> 1;
+                const int stage = j % kKStages, round = j / kKStages;
                 const int vst = j % kVStages, vrd = j / kVStages;
                 if constexpr (kTma) {
                     const int nseg = (valid + p.box_rows - 1) / p.box_rows;
