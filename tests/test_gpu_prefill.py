@@ -19,7 +19,9 @@ def bsp():
 CASES = [
     # (seed, qo lens, kv lens, H_qo, H_kv, page, causal, num_ctas)
     (1, [1, 17, 128, 129, 300], [1, 17, 128, 129, 300], 32, 8, 16, True, 152),
-    (2, [200, 64, 1000], [200, 64, 1000], 32, 8, 16, True, 7),           # splits + merges
+    (2, [200, 64, 1000], [200, 64, 1000], 32, 8, 16, True, 7),           # few CTAs, long queues
+    (12, [200, 64, 1000], [200, 64, 1000], 32, 8, 16, True, 200),        # splits + merges (48 entries)
+    (11, [64, 5, 100], [6000, 700, 3000], 32, 8, 16, True, 40),         # prefix cached: splits + merges
     (3, [33, 5, 260], [100, 5, 900], 8, 8, 8, True, 13),                 # qo < kv (prefix cached)
     (4, [70, 300], [20, 128], 16, 2, 32, True, 5),                       # qo > kv: rows with no key
     (5, [64, 190, 3], [500, 190, 77], 16, 16, 128, False, 9),            # non-causal, g = 1
@@ -38,6 +40,33 @@ def test_random_prefill(bsp, case):
     O, L = oracle_full(b)
     out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=C)
     compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_split_prefill_repeated_runs(bsp):
+    """Split prefill (24 reduction-map entries): three runs of one plan give
+    identical results that match the oracle, and one more merge-of-partials
+    launch afterwards changes nothing (it recomputes the same fold)."""
+    import ctypes
+    from block_sparse_paged_gb300 import _native as N
+    b = workloads.paged_batch(82, [64, 5, 100], [6000, 700, 3000], 32, 8, 128, 16, "bf16", causal=True,
+                              extra_pages=2)
+    dev = to_dev(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=40, dev_tensors=dev)
+    assert pa.info.num_merges > 0
+    q, k, v, idx = dev
+    runs = [pa.run(q, k, v, idx, b.sm_scale) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o2, l2 in runs:
+        assert torch.equal(o2, out) and torch.equal(l2, lse)
+    O, L = oracle_full(b)
+    compare(out, lse, O, L, "bf16")
+    o3, l3 = out.clone(), lse.clone()
+    N.check(N.load().bsp_run_merge_partials(ctypes.byref(pa.info), ctypes.c_void_p(o3.data_ptr()),
+                                            ctypes.c_void_p(l3.data_ptr()), ctypes.c_void_p(pa.workspace.data_ptr()),
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    torch.cuda.synchronize()
+    assert torch.equal(o3, out) and torch.equal(l3, lse)
     assert pa.check_device_error() == 0
 
 

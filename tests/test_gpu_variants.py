@@ -102,7 +102,7 @@ SINK_PREFILL = [
     # through the merge kernel, whole rows through the epilogue
     (124, [300, 65, 1000], [300, 65, 1000], 32, 8, 16, True, -1, 13),
     (125, [200, 90], [700, 90], 16, 4, 1, True, 77, 7),
-    (126, [128, 300], [128, 500], 32, 8, 32, False, -1, 40),
+    (126, [128, 300], [128, 500], 32, 8, 32, False, -1, 80),   # 40 merge entries
 ]
 
 
