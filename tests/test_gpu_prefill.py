@@ -114,6 +114,41 @@ def test_shared_prefix_composable_small(bsp):
     compare(out, lse, O, L, "bf16")
 
 
+def test_shared_prefix_concurrent_views(bsp):
+    """The two views on two streams at once, each on part of the SMs (their plans
+    made for those CTA counts), give bit-for-bit the outputs of the same plans
+    run one after the other, and those match the oracle."""
+    sp = workloads.shared_prefix_decode_bf16(batch=8, prefix_len=1024, outlier=3000, seed=12)
+    dev = torch.device("cuda")
+    q, k, v = sp.full.q.to(dev), sp.full.k_pages.to(dev), sp.full.v_pages.to(dev)
+    ip = torch.from_numpy(sp.prefix.kv_indices).to(dev)
+    isf = torch.from_numpy(sp.suffix.kv_indices).to(dev)
+    pre = bsp.PagedAttention("prefill", 32, 8, 128, sp.full.page_size, False, torch.bfloat16, max_batch=1,
+                             max_qo_tokens=int(sp.prefix.qo_indptr[-1]), num_ctas=50)
+    suf = bsp.PagedAttention("decode", 32, 8, 128, sp.full.page_size, False, torch.bfloat16,
+                             max_batch=sp.suffix.batch, num_ctas=102)
+    pre.plan(sp.prefix.kv_indptr, sp.prefix.last_page_len, qo_indptr=sp.prefix.qo_indptr)
+    suf.plan(sp.suffix.kv_indptr, sp.suffix.last_page_len)
+    o1, l1 = pre.run(q, k, v, ip, sp.full.sm_scale)
+    o2, l2 = suf.run(q, k, v, isf, sp.full.sm_scale)
+    ref_o, ref_l = bsp.merge_state(o1, l1, o2, l2)
+    torch.cuda.synchronize()
+    main, sa, sb = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    c1, c2 = torch.empty_like(o1), torch.empty_like(o2)
+    d1, d2 = torch.empty_like(l1), torch.empty_like(l2)
+    sa.wait_stream(main)
+    sb.wait_stream(main)
+    pre.run(q, k, v, ip, sp.full.sm_scale, out=c1, lse=d1, stream=sa)
+    suf.run(q, k, v, isf, sp.full.sm_scale, out=c2, lse=d2, stream=sb)
+    main.wait_stream(sa)
+    main.wait_stream(sb)
+    out, lse = bsp.merge_state(c1, d1, c2, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    O, L = oracle_full(sp.full)
+    compare(out, lse, O, L, "bf16")
+
+
 def test_shared_prefix_composable_full_size(bsp):
     """64 requests sharing an 8192-token prefix, suffixes U{64..1024} and one
     32768 outlier: prefix view + suffix view + merge equals attention over the
