@@ -89,9 +89,13 @@ struct DecodeLayout {
     // kFp8: 128-token stages (half the bytes per token, so the same bytes per
     // stage and per barrier round trip) shared by 8 compute warps, two per
     // scheduler, so that each hides the other's latency
-    static constexpr int kTK = kFp8 ? 2 * kTileK : kTileK;   // KV tokens per stage, 16 per compute warp
-    static constexpr int kS = kStages;                       // ring stages
-    static constexpr int kCons = kTK / 16;                   // compute warps
+    // bf16 with TMA: 128-token stages too (64 KB), 3 of them, each of the 4
+    // compute warps taking two 16-token sub-blocks per stage. Fewer, larger
+    // stages: a stage's fixed handshake cost is spread over more bytes.
+    static constexpr int kTK = (kFp8 || kTma) ? 2 * kTileK : kTileK;  // KV tokens per stage
+    static constexpr int kS = (kTma && !kFp8) ? 3 : kStages;            // ring stages
+    static constexpr int kCons = kFp8 ? 8 : 4;                           // compute warps
+    static constexpr int kSubB = kTK / (16 * kCons);                     // 16-token sub-blocks per warp and stage
     static constexpr int kThreads = 32 * (kCons + 2);
     static constexpr int kElem = kFp8 ? 1 : 2;               // bytes per K/V element in the ring
     static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 128-byte-wide slab
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const DecodeParams p) {
     static_assert(!kFp8 || (kTma && D == 128), "e4m3 pools: TMA gather, head_dim 128");
+    static_assert(!kFp8 || DecodeLayout<D, kTma, kFp8>::kSubB == 1, "e4m3: one 16-token block per warp and stage");
     using LY = DecodeLayout<D, kTma, kFp8>;
     constexpr int kStages = LY::kS;
     constexpr int kConsumers = LY::kCons;
@@ -565,11 +570,14 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 const int s = k % kStages;
                 const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
                 if (!__all_sync(0xffffffffu, ok)) return;
-                const int valid = min(kTK, len - t * kTK) - warp * 16;  // this warp's tokens
+#pragma unroll 1
+                for (int sbk = 0; sbk < LY::kSubB; ++sbk) {
+                const int row0 = (sbk * kConsumers + warp) * 16;        // this sub-block's first stage row
+                const int valid = min(kTK, len - t * kTK) - row0;      // its tokens
                 // sliding window: tokens of this warp before the window's edge (the chunk
                 // starts on a page boundary at or before it) are masked
                 const int lo_rel = p.window_left > 0
-                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + warp * 16)
+                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + row0)
                                        : INT_MIN;
                 if (valid > 0) {
                     const uint32_t kb = sbase + s * LY::kStageBytes;
@@ -578,7 +586,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                         // whole page boxes were copied: V rows of this warp past the chunk
                         // end may hold anything; zero them so that P = 0 meets finite values
                         for (int e = lane; e < (16 - valid) * (D / 8); e += 32) {
-                            const int row = warp * 16 + valid + e / (D / 8);
+                            const int row = row0 + valid + e / (D / 8);
                             *reinterpret_cast<uint4 *>(smem + (vb - sbase) + LY::chunk(row, e % (D / 8))) =
                                 make_uint4(0, 0, 0, 0);
                         }
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                     for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
                     {
                         const int mi = lane >> 3;
-                        const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+                        const int row = row0 + (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             uint32_t b0, b1, b2, b3;
@@ -647,7 +655,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                     pa[3] = pack_bf16(ps[1][2], ps[1][3]);
                     {
                         const int mi = lane >> 3;
-                        const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
+                        const int row = row0 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
                         for (int nd = 0; nd < D / 16; ++nd) {
                             uint32_t b0, b1, b2, b3;
@@ -657,6 +665,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                         }
                     }
                 }
+                }  // sub-blocks
                 if (kTma) sm100::fence_proxy_async_smem();  // generic writes above before the next tensor copy
                 __syncwarp();
                 if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
