@@ -84,7 +84,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // kFp8 (with kTma, D = 128): the ring holds e4m3 rows (128 bytes, one swizzle
 // row); the compute warps read the bytes straight into f16 tensor-core
 // fragments (no staging copy).
-template <int D, bool kTma, bool kFp8 = false>
+template <int D, bool kTma, bool kFp8 = false, int kNH = 1>
 struct DecodeLayout {
     // kFp8: 128-token stages (half the bytes per token, so the same bytes per
     // stage and per barrier round trip) shared by 8 compute warps, two per
@@ -92,10 +92,13 @@ struct DecodeLayout {
     // bf16 with TMA: 128-token stages too (64 KB), 3 of them, each of the 4
     // compute warps taking two 16-token sub-blocks per stage. Fewer, larger
     // stages: a stage's fixed handshake cost is spread over more bytes.
-    static constexpr int kTK = (kFp8 || kTma) ? 2 * kTileK : kTileK;  // KV tokens per stage
-    static constexpr int kS = (kTma && !kFp8) ? 3 : kStages;            // ring stages
-    static constexpr int kCons = kFp8 ? 8 : 4;                           // compute warps
-    static constexpr int kSubB = kTK / (16 * kCons);                     // 16-token sub-blocks per warp and stage
+    // e4m3 with g <= 8: 256-token stages (64 KB), 3 of them, two sub-blocks per
+    // warp (the head-major scratch needs only 8 rows per warp then).
+    static constexpr int kTK = kFp8 ? (kNH == 1 ? 4 * kTileK : 2 * kTileK) : kTma ? 2 * kTileK : kTileK;
+    static constexpr int kS = (kTma && !(kFp8 && kNH == 2)) ? 3 : kStages;  // ring stages
+    static constexpr int kCons = kFp8 ? 8 : 4;                               // compute warps
+    static constexpr int kSubB = kTK / (16 * kCons);                         // 16-token sub-blocks per warp and stage
+    static constexpr int kScrRows = kFp8 ? 8 * kNH : kMmaRows;               // scratch rows per warp
     static constexpr int kThreads = 32 * (kCons + 2);
     static constexpr int kElem = kFp8 ? 1 : 2;               // bytes per K/V element in the ring
     static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 128-byte-wide slab
@@ -104,8 +107,8 @@ struct DecodeLayout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kS * kStageBytes;
     static constexpr int kScratchOff = kRingBytes;
-    static constexpr int kScratchBytes = kCons * kMmaRows * D * 4;   // per-warp O rows for the item merge
-    static constexpr int kStatBytes = kCons * kMmaRows * 2 * 4;      // per-warp (m, l)
+    static constexpr int kScratchBytes = kCons * kScrRows * D * 4;   // per-warp O rows for the item merge
+    static constexpr int kStatBytes = kCons * kScrRows * 2 * 4;      // per-warp (m, l)
     static constexpr int kBarOff = kScratchOff + kScratchBytes + kStatBytes;
     static constexpr int kNumBars = 2 * kS + 3;             // full[S], empty[S], merge_in, merge_out, last
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
@@ -205,8 +208,8 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const DecodeParams p) {
     static_assert(!kFp8 || (kTma && D == 128), "e4m3 pools: TMA gather, head_dim 128");
-    static_assert(!kFp8 || DecodeLayout<D, kTma, kFp8>::kSubB == 1, "e4m3: one 16-token block per warp and stage");
-    using LY = DecodeLayout<D, kTma, kFp8>;
+    using LY = DecodeLayout<D, kTma, kFp8, kNH>;
+    constexpr int kSR = LY::kScrRows;
     constexpr int kStages = LY::kS;
     constexpr int kConsumers = LY::kCons;
     constexpr int kWsThreads = LY::kThreads;
@@ -409,13 +412,19 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 const int s = k % kStages;
                 const bool ok = wait_or_abort(full0 + 8 * s, (k / kStages) & 1, abort_flag, status, kStatusConsumerWait);
                 if (!__all_sync(0xffffffffu, ok)) return;
-                const int valid = min(kTK, len - t * kTK) - warp * 16;  // this warp's tokens
+#pragma unroll 1
+                for (int sbk = 0; sbk < LY::kSubB; ++sbk) {
+                const int row0 = (sbk * kConsumers + warp) * 16;        // this sub-block's first stage row
+                const bool last_sb = sbk == LY::kSubB - 1;               // the stage goes back after its loads
+                const int valid = min(kTK, len - t * kTK) - row0;      // its tokens
                 const int lo_rel = p.window_left > 0
-                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + warp * 16)
+                                       ? w.pos0 + w.kv_len - w.qo_len - p.window_left - (w.kv_start + t * kTK + row0)
                                        : INT_MIN;
-                if (valid <= 0) {
-                    __syncwarp();
-                    if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+                if (valid <= 0) {  // so are the later sub-blocks'
+                    if (last_sb) {
+                        __syncwarp();
+                        if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+                    }
                     continue;
                 }
                 const uint32_t kb = sbase + s * LY::kStageBytes, vb = kb + LY::kTileBytes;
@@ -426,12 +435,12 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int R = warp * 16 + 8 * t2 + qn;
+                        const int R = row0 + 8 * t2 + qn;
                         kw[t2][h] = sm100::ld_shared_v4(kb + R * 128 + (((4 * h + c) ^ (R & 7)) << 4));
                     }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = warp * 16 + rr;
+                    const int rr = 2 * c + (i & 1) + 8 * (i >> 1), R = row0 + rr;
                     vw[i] = sm100::ld_shared_v4(vb + R * 128 + ((qn ^ (R & 7)) << 4));
                 }
                 if (valid < 16) {  // the chunk ends inside this warp's rows (warp-uniform)
@@ -439,8 +448,10 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                     for (int i = 0; i < 4; ++i)
                         if (2 * c + (i & 1) + 8 * (i >> 1) >= valid) vw[i] = make_uint4(0, 0, 0, 0);
                 }
-                __syncwarp();
-                if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+                if (last_sb) {
+                    __syncwarp();
+                    if (lane == 0) sm100::mbar_arrive(empty0 + 8 * s);
+                }
 
                 // S^T: two accumulators per head tile (even / odd kk) to halve the chain
                 float st[kNH][2][4];
@@ -517,6 +528,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                         mma_f16_16816(oacc[2 * m + 1][nh], a_o, pb[nh][0], pb[nh][1]);
                     }
                 }
+                }  // sub-blocks
             }
 
             // ---- this warp's state per head -> stats / scratch rows (heads) ----
@@ -529,12 +541,12 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 }
                 const int h0 = 8 * nh + 2 * c;
                 if (qn == 0) {
-                    stats[(warp * 16 + h0) * 2 + 0] = mh[nh][0];
-                    stats[(warp * 16 + h0) * 2 + 1] = lh[nh][0];
-                    stats[(warp * 16 + h0 + 1) * 2 + 0] = mh[nh][1];
-                    stats[(warp * 16 + h0 + 1) * 2 + 1] = lh[nh][1];
+                    stats[(warp * kSR + h0) * 2 + 0] = mh[nh][0];
+                    stats[(warp * kSR + h0) * 2 + 1] = lh[nh][0];
+                    stats[(warp * kSR + h0 + 1) * 2 + 0] = mh[nh][1];
+                    stats[(warp * kSR + h0 + 1) * 2 + 1] = lh[nh][1];
                 }
-                float *s0 = scratch + (warp * 16 + h0) * D + 16 * qn;
+                float *s0 = scratch + (warp * kSR + h0) * D + 16 * qn;
                 float *s1 = s0 + D;
 #pragma unroll
                 for (int i = 0; i < D / 32; ++i) {
@@ -677,16 +689,16 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             if ((lane & 3) == 0) {
-                stats[(warp * 16 + r0) * 2 + 0] = m0;
-                stats[(warp * 16 + r0) * 2 + 1] = l0;
-                stats[(warp * 16 + r1) * 2 + 0] = m1;
-                stats[(warp * 16 + r1) * 2 + 1] = l1;
+                stats[(warp * kSR + r0) * 2 + 0] = m0;
+                stats[(warp * kSR + r0) * 2 + 1] = l0;
+                stats[(warp * kSR + r1) * 2 + 0] = m1;
+                stats[(warp * kSR + r1) * 2 + 1] = l1;
             }
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
                 const int col = n * 8 + 2 * (lane & 3);
-                *reinterpret_cast<float2 *>(scratch + (warp * 16 + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
-                *reinterpret_cast<float2 *>(scratch + (warp * 16 + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
+                *reinterpret_cast<float2 *>(scratch + (warp * kSR + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
+                *reinterpret_cast<float2 *>(scratch + (warp * kSR + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
             }
         }
         __syncwarp();
@@ -696,15 +708,15 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             const int row = e / D, d = e - row * D;
             float M = -INFINITY;
 #pragma unroll
-            for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, stats[(ww * 16 + row) * 2]);
+            for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, stats[(ww * kSR + row) * 2]);
             float val = 0.f, lse_v = -INFINITY;
             if (M != -INFINITY) {
                 float L = 0.f, num = 0.f;
 #pragma unroll
                 for (int ww = 0; ww < kConsumers; ++ww) {
-                    const float f = exp2f(stats[(ww * 16 + row) * 2] - M);
-                    L += stats[(ww * 16 + row) * 2 + 1] * f;
-                    num += scratch[(ww * 16 + row) * D + d] * f;
+                    const float f = exp2f(stats[(ww * kSR + row) * 2] - M);
+                    L += stats[(ww * kSR + row) * 2 + 1] * f;
+                    num += scratch[(ww * kSR + row) * D + d] * f;
                 }
                 val = num / L * p.v_scale;
                 lse_v = (M + log2f(L)) * kLn2;
@@ -895,14 +907,14 @@ int launch_decode_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const Decod
     static bool configured[64] = {false};
     int dev = 0;
     if (num_sms_of_current_device(&dev) < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
-    constexpr int kSmem = DecodeLayout<D, kTma, kFp8>::kSmemBytes;
+    constexpr int kSmem = DecodeLayout<D, kTma, kFp8, kNH>::kSmemBytes;
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D, kTma, kFp8, kNH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode smem attribute: ") + cudaGetErrorString(e));
         configured[dev] = true;
     }
-    decode_bf16_kernel<D, kTma, kFp8, kNH><<<grid, DecodeLayout<D, kTma, kFp8>::kThreads, kSmem, stream>>>(tk, tv, p);
+    decode_bf16_kernel<D, kTma, kFp8, kNH><<<grid, DecodeLayout<D, kTma, kFp8, kNH>::kThreads, kSmem, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
     return BSP_OK;
