@@ -113,7 +113,12 @@ typedef struct bsp_problem {
  * persistent buffers sized to declared bounds; exceeding them is an error). */
 typedef struct bsp_capacity {
     int32_t max_batch;      /* requests per plan                                  */
-    int32_t num_ctas;       /* persistent CTAs of the attention kernel (C)        */
+    int32_t num_ctas;       /* plan queues C: the LPT plan balances C queues. The
+                               kernels launch min(C, R) CTAs for R resident CTAs
+                               of the device when C is a multiple of R or at most
+                               R; otherwise each CTA runs ceil(C / R) consecutive
+                               queues, so C = R + 1 .. 2R - 1 leaves SMs idle:
+                               prefer R (bsp_default_num_ctas) or a multiple  */
     int64_t max_qo_tokens;  /* total query positions per plan                     */
 } bsp_capacity;
 
