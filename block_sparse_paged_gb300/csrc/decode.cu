@@ -89,13 +89,14 @@ struct DecodeLayout {
     // kFp8: 128-token stages (half the bytes per token, so the same bytes per
     // stage and per barrier round trip) shared by 8 compute warps, two per
     // scheduler, so that each hides the other's latency
-    // bf16 with TMA: 128-token stages too (64 KB), 3 of them, each of the 4
-    // compute warps taking two 16-token sub-blocks per stage. Fewer, larger
-    // stages: a stage's fixed handshake cost is spread over more bytes.
+    // bf16: 128-token stages too, each of the 4 compute warps taking two
+    // 16-token sub-blocks per stage: 3 stages of 64 KB with TMA, 2 of 68 KB
+    // (padded rows) with cp.async. Fewer, larger stages: a stage's fixed
+    // handshake cost is spread over more bytes.
     // e4m3 with g <= 8: 256-token stages (64 KB), 3 of them, two sub-blocks per
     // warp (the head-major scratch needs only 8 rows per warp then).
-    static constexpr int kTK = kFp8 ? (kNH == 1 ? 4 * kTileK : 2 * kTileK) : kTma ? 2 * kTileK : kTileK;
-    static constexpr int kS = (kTma && !(kFp8 && kNH == 2)) ? 3 : kStages;  // ring stages
+    static constexpr int kTK = kFp8 ? (kNH == 1 ? 4 * kTileK : 2 * kTileK) : 2 * kTileK;
+    static constexpr int kS = kTma ? ((kFp8 && kNH == 2) ? kStages : 3) : 2;  // ring stages
     static constexpr int kCons = kFp8 ? 8 : 4;                               // compute warps
     static constexpr int kSubB = kTK / (16 * kCons);                         // 16-token sub-blocks per warp and stage
     static constexpr int kScrRows = kFp8 ? 8 * kNH : kMmaRows;               // scratch rows per warp
@@ -318,23 +319,26 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
         for (int it = it0; it < it1 && !*abort_flag; ++it) {
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
-            const int nt = (len + kTileK - 1) / kTileK;
-            int pg[2] = {0, 0};
-            auto fetch = [&](int t, int (&dst)[2]) {
+            const int nt = (len + kTK - 1) / kTK;
+            constexpr int kJ = kTK / 32;  // tokens per lane and stage
+            int pg[kJ];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
+            for (int jj = 0; jj < kJ; ++jj) pg[jj] = 0;
+            auto fetch = [&](int t, int (&dst)[kJ]) {
+#pragma unroll
+                for (int jj = 0; jj < kJ; ++jj) {
                     const int j = lane + 32 * jj;
-                    const int tok = w.kv_start + t * kTileK + j;
-                    if (t * kTileK + j < len) dst[jj] = __ldg(p.kv_indices + w.page_base + tok / p.page_size);
+                    const int tok = w.kv_start + t * kTK + j;
+                    if (t * kTK + j < len) dst[jj] = __ldg(p.kv_indices + w.page_base + tok / p.page_size);
                 }
             };
             if (nt > 0) fetch(0, pg);
             for (int t = 0; t < nt; ++t, ++k) {
                 // byte offsets of this lane's two rows, then the next tile's page ids
-                uint64_t off[2];
+                uint64_t off[kJ];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int tok = w.kv_start + t * kTileK + lane + 32 * jj;
+                for (int jj = 0; jj < kJ; ++jj) {
+                    const int tok = w.kv_start + t * kTK + lane + 32 * jj;
                     off[jj] = (((uint64_t)pg[jj] * p.page_size + tok % p.page_size) * p.H_kv + w.kv_head) * (D * 2);
                 }
                 if (t + 1 < nt) fetch(t + 1, pg);
@@ -342,10 +346,10 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 const bool ok = wait_or_abort(empty0 + 8 * s, ((k / kStages) & 1) ^ 1, abort_flag, status,
                                               kStatusProducerWait);
                 if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: every lane leaves together
-                const int n = min(kTileK, len - t * kTileK);
+                const int n = min(kTK, len - t * kTK);
                 const uint32_t dst = sbase + s * LY::kStageBytes + part + (uint32_t)my_chunk * 16;
 #pragma unroll
-                for (int i = 0; i < kTileK / T; ++i) {
+                for (int i = 0; i < kTK / T; ++i) {
                     const int j = i * T + my_sub;                     // token within the stage
                     const int half = (i * T) >> 5;                    // same for the whole warp: T divides 32
                     const uint64_t o = __shfl_sync(0xffffffffu, off[half], j & 31);
