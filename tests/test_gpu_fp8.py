@@ -114,3 +114,61 @@ def test_fp8_rejects_bad_scales_and_shapes(bsp):
     b4 = workloads.paged_batch(111, [1, 1], [100, 50], 32, 8, 128, 4, "bf16")
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         run_fp8(bsp, b4, workloads.fp8_kv(b4))
+
+
+def test_fp8_graph_replay_with_sink(bsp):
+    """An e4m3 decode run with sinks captured in a CUDA graph, then replayed
+    after a re-plan of other requests loaded into the same pools (one scale
+    pair for both, as the captured launch holds the scales): both replays
+    match the oracle."""
+    a = workloads.paged_batch(113, [1] * 5, [3000, 17, 900, 0, 2200], 32, 8, 128, 16, "bf16", extra_pages=3)
+    bb = workloads.paged_batch(114, [1] * 5, [50, 4000, 1, 700, 1300], 32, 8, 128, 16, "bf16", extra_pages=3)
+
+    def amax(t):
+        return float(torch.nan_to_num(t.float(), nan=0.0).abs().max())
+    ks = max(amax(a.k_pages), amax(bb.k_pages)) / 448.0
+    vs = max(amax(a.v_pages), amax(bb.v_pages)) / 448.0
+    codes = {id(b): ((b.k_pages.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8),
+                     (b.v_pages.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)) for b in (a, bb)}
+    sk = np.random.default_rng(113).uniform(-2.0, 4.0, size=32)
+    pool = max(a.k_pages.shape[0], bb.k_pages.shape[0])
+    k8 = torch.zeros((pool, 16, 8, 128), dtype=torch.uint8, device="cuda")
+    v8 = torch.zeros_like(k8)
+    q = torch.empty_like(a.q, device="cuda")
+    idx = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    sink = torch.tensor(sk, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+
+    def load(b):
+        kc, vc = codes[id(b)]
+        k8[: kc.shape[0]].copy_(kc)
+        v8[: vc.shape[0]].copy_(vc)
+        q.copy_(b.q)
+        idx[: len(b.kv_indices)].copy_(torch.from_numpy(np.ascontiguousarray(b.kv_indices, np.int32)))
+
+    pa = bsp.PagedAttention("decode", 32, 8, 128, 16, False, torch.bfloat16, max_batch=5, num_ctas=19)
+    kf, vf = k8.view(torch.float8_e4m3fn), v8.view(torch.float8_e4m3fn)
+
+    def run():
+        pa.run(q, kf, vf, idx, a.sm_scale, out=out, lse=lse, k_scale=ks, v_scale=vs, sink=sink)
+    load(a)
+    pa.plan(a.kv_indptr, a.last_page_len)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()  # warm up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for b in (a, bb):
+        if b is bb:
+            load(bb)
+            pa.plan(bb.kv_indptr, bb.last_page_len)
+        g.replay()
+        torch.cuda.synchronize()
+        kc, vc = codes[id(b)]
+        O, L = oracle.attention_of(b, k=oracle.fp8.dequantize(kc.numpy(), ks),
+                                   v=oracle.fp8.dequantize(vc.numpy(), vs), sink=sk)
+        compare(out, lse, O, L, "bf16")

@@ -70,6 +70,56 @@ def test_split_prefill_repeated_runs(bsp):
     assert pa.check_device_error() == 0
 
 
+def test_prefill_cuda_graph_replay_with_new_plan(bsp):
+    """Capture one prefill run (attention kernel + merge of partials), re-plan
+    other lengths into the same workspace and replay: the replay matches the
+    oracle for the new plan. Both plans split outputs."""
+    hq, hk, ps = 32, 8, 16
+    a = workloads.paged_batch(61, [64, 5, 100], [6000, 700, 3000], hq, hk, 128, ps, "bf16", causal=True,
+                              extra_pages=30)
+    bb = workloads.paged_batch(62, [7, 64, 90], [2500, 5200, 90], hq, hk, 128, ps, "bf16", causal=True,
+                               extra_pages=30)
+    pa = bsp.PagedAttention("prefill", hq, hk, 128, ps, True, torch.bfloat16, max_batch=3, max_qo_tokens=256,
+                            num_ctas=40)
+    pool = max(a.k_pages.shape[0], bb.k_pages.shape[0])
+    n_tok = max(int(a.qo_indptr[-1]), int(bb.qo_indptr[-1]))
+    q = torch.zeros((n_tok, hq, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((pool, ps, hk, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    idx = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+
+    def load(batch):
+        q[: batch.q.shape[0]].copy_(batch.q)
+        k[: batch.k_pages.shape[0]].copy_(batch.k_pages)
+        v[: batch.v_pages.shape[0]].copy_(batch.v_pages)
+        idx[: len(batch.kv_indices)].copy_(torch.from_numpy(batch.kv_indices))
+
+    load(a)
+    pa.plan(a.kv_indptr, a.last_page_len, qo_indptr=a.qo_indptr)
+    assert pa.info.num_merges > 0
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.run(q, k, v, idx, a.sm_scale, out=out, lse=lse)  # warm up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.run(q, k, v, idx, a.sm_scale, out=out, lse=lse)
+    for batch in (a, bb):
+        if batch is bb:
+            load(bb)
+            pa.plan(bb.kv_indptr, bb.last_page_len, qo_indptr=bb.qo_indptr)
+            assert pa.info.num_merges > 0
+        g.replay()
+        torch.cuda.synchronize()
+        O, L = oracle_full(batch)
+        n = int(batch.qo_indptr[-1])
+        compare(out[:n], lse[:n], O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
 def test_ragged_causal_prefill_full_size(bsp):
     """16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, causal;
     sampled rows against the oracle; two runs bitwise equal."""
