@@ -6,29 +6,40 @@
 // every byte of K and V is read once, and the g heads that share a kv head reuse
 // each loaded KV tile (head-group fusion, technical review eq 3; overview ⑦).
 //
-// bf16 kernel (one persistent CTA per plan queue, one CTA per SM):
-//   - loaders (warp 4: K, warp 5: V): 16-byte cp.async copies addressed
-//     through the page table, each warp instruction covering two whole
-//     256-byte rows; each lane computes two row offsets per stage
-//     (sparse gather, dense compute: overview ⑥, walkthrough §IV.2 and §V.4),
-//     into a 5-stage ring of 64-token stages with padded rows; page indices
-//     are fetched one stage ahead and shared by shuffles. mbarriers carry the
-//     handshake (full: every producer lane's copies landed, through
-//     cp.async.mbarrier.arrive; empty: the four compute warps are done with
-//     the stage), and the ring runs across the CTA's work items, so the next
-//     item's first stages load while the current one finishes.
-//   - compute (warps 0..3): each warp takes 16 of the 64 tokens; S = Q K^T and
-//     O += P V on the warp-level tensor-core MMA (m16n8k16, rows = the g fused
-//     heads), fp32 online softmax in base 2 with the scale folded into
-//     log2(e) (walkthrough §II.2); at the end of each item the four warps'
+// bf16 kernel (one persistent CTA per SM, running its plan queue(s)):
+//   - loaders (warp 4: K, warp 5: V) fill a ring of stages through the page
+//     table (sparse gather, dense compute: overview ⑥, walkthrough §IV.2 and
+//     §V.4). Pages of 8 or more tokens: one TMA tensor copy per page box
+//     (up to 64 rows of one kv head, 128-byte swizzle), page ids read 32 boxes
+//     at a time one batch ahead; 3 stages of 128 tokens. Smaller pages: 16-byte
+//     cp.async copies into padded rows, 2 stages of 128 tokens. Stages are large
+//     because each carries a fixed handshake cost. mbarriers carry the
+//     handshake (full: the stage's bytes / every lane's copies landed; empty:
+//     the compute warps are done with it); the ring runs across the CTA's work
+//     items, so the next item's first stages load while the current one ends.
+//   - compute (warps 0..3): each warp takes two 16-token sub-blocks per stage;
+//     S = Q K^T and O += P V on the warp-level tensor-core MMA (m16n8k16, rows
+//     = the g fused heads), fp32 online softmax in base 2 with the scale folded
+//     into log2(e) (walkthrough §II.2); at the end of each item the warps'
 //     states are merged in shared memory.
-//   - output: the final (O, LSE) when the item is its output's only chunk,
-//     else an fp32 partial state in the workspace slot the plan assigned
-//     (overview ⑨, write-through of unsplit requests).
-//   - every wait is a bounded spin (SM clock cycles); a wait that gives up sets the workspace
-//     status word and an abort flag the other warps see, and the CTA returns.
+//   - output: the final (O, LSE) when the item is its output's only chunk, else
+//     an fp32 partial state in the workspace slot the plan assigned (overview
+//     ⑨). A partial is counted in its reduction-map entry with an atomic after
+//     a device-scope fence; the CTA whose partial completes the count folds the
+//     entry (slots in order, one common maximum) and resets the count, so no
+//     CTA ever waits for another and a run is one launch.
+//   - every wait is a bounded spin (SM clock cycles); a wait that gives up sets
+//     the workspace status word and an abort flag the other warps see, and the
+//     CTA returns.
+// e4m3 kernel (the same template, kFp8): K / V pools of e4m3 codes (FlashInfer:
+// A Customizable Attention Engine for LLM Serving, App. G.4 Table 8), 8 compute
+// warps, 256-token stages; codes go from shared memory straight into f16
+// fragments of transposed tiles (S^T = K Q^T, O^T = V^T P^T: tokens on the MMA's
+// M side, P^T by movmatrix).
+// fp32 kernel: CUDA cores, fp32 throughout, same plan and merge.
 // Reduction kernel: the reduction map's slots of each split output, merged in
-// ascending order with a common maximum (technical review eq 6), no atomics.
+// ascending order with a common maximum (technical review eq 6); used after the
+// prefill kernel and by bsp_run_merge_partials.
 #include <cfloat>
 #include <cmath>
 #include <climits>
@@ -51,7 +62,7 @@ constexpr int kMmaRows = 16;                 // fused heads per tile (M of the M
 
 // bf16 kernel: warps 0..3 compute, warps 4 and 5 load K and V.
 constexpr int kConsumers = 4;
-constexpr int kTileK = 64;                   // KV tokens per ring stage (16 per consumer warp)
+constexpr int kTileK = 64;                   // unit of the stage sizes below; the largest page box (rows)
 constexpr int kStages = 5;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
 
@@ -955,7 +966,7 @@ int launch_reduce_t(const ReduceParams &p, cudaStream_t stream) {
 
 int decode_ctas_per_sm(int head_dim, int dtype) {
     if (dtype != BSP_DTYPE_BF16) return 4;
-    return 1;  // a 5-stage ring of 64-token K+V stages (~174 KB at D = 128) per SM
+    return 1;  // a ring of 128-token K+V stages and the merge scratch fill an SM's shared memory
 }
 
 namespace {
