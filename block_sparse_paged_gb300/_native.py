@@ -31,7 +31,7 @@ _ERR_NAMES = {BSP_ERR_INVALID_ARG: "INVALID_ARG", BSP_ERR_CAPACITY: "CAPACITY", 
 
 EXPORTED = ["bsp_default_num_ctas", "bsp_workspace_size", "bsp_host_staging_size", "bsp_plan",
             "bsp_decode_run", "bsp_decode_run_fp8", "bsp_prefill_run", "bsp_run_attention", "bsp_run_merge_partials",
-            "bsp_merge_state", "bsp_decode_run_static", "bsp_check_device_error",
+            "bsp_merge_state", "bsp_decode_run_static", "bsp_check_device_error", "bsp_check_bounded_wait",
             "bsp_last_error", "bsp_version"]
 
 
@@ -102,6 +102,7 @@ def load():
         "bsp_merge_state": ([vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp], ctypes.c_int),
         "bsp_decode_run_static": ([PI, vp, vp, vp, vp, vp, f32, vp, vp, vp], ctypes.c_int),
         "bsp_check_device_error": ([PI, vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "bsp_check_bounded_wait": ([i64, vp, vp], ctypes.c_int),
         "bsp_last_error": ([], ctypes.c_char_p),
         "bsp_version": ([], ctypes.c_char_p),
     }

@@ -126,6 +126,14 @@ extern "C" int bsp_run_merge_partials(const bsp_plan_info *plan, void *o, float 
     return launch_reduce(plan, o, lse, workspace, stream);
 }
 
+extern "C" int bsp_check_bounded_wait(int64_t limit_cycles, int32_t *status, bsp_stream_t stream) {
+    clear_error();
+    if (!status) return fail(BSP_ERR_INVALID_ARG, "status is NULL");
+    if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 33))
+        return fail(BSP_ERR_INVALID_ARG, "limit_cycles must be in [1, 2^33] (about 4 s)");
+    return launch_wait_probe(limit_cycles, reinterpret_cast<int *>(status), stream);
+}
+
 extern "C" int bsp_merge_state(const void *o_a, const float *lse_a, const void *o_b, const float *lse_b, void *o_out,
                                float *lse_out, int64_t n_rows, int32_t num_heads, int32_t head_dim, int32_t dtype,
                                bsp_stream_t stream) {

@@ -75,6 +75,7 @@ int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pa
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages,
                    const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
                    float sm_scale, void *o, float *lse, void *workspace, cudaStream_t stream);
+int launch_wait_probe(long long limit_cycles, int *status, cudaStream_t stream);
 int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace,
                   cudaStream_t stream);
 int launch_merge_state(const void *o_a, const float *lse_a, const void *o_b, const float *lse_b,

@@ -202,6 +202,7 @@ __device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_mer
 constexpr int kStatusProducerWait = 0x101;
 constexpr int kStatusConsumerWait = 0x102;
 constexpr int kStatusMergeWait = 0x103;
+constexpr int kStatusProbeWait = 0x1ff;  // wait_probe_kernel
 
 // Bounded mbarrier wait that also gives up as soon as another warp aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
@@ -212,6 +213,23 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
         atomicCAS(status, 0, code);
     }
     return false;
+}
+
+// One warp waits, with the kernels' bounded spin, on an mbarrier that nothing
+// arrives at: the wait gives up after limit_cycles and records the probe code
+// in *status the way every kernel wait does (used to test that path).
+__global__ void wait_probe_kernel(long long limit_cycles, int *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(b, 1);
+        abort_flag = 0;
+        sm100::fence_barrier_init();
+    }
+    __syncthreads();
+    if (!sm100::mbar_wait_spin(b, 0, limit_cycles, &abort_flag) && threadIdx.x == 0)
+        atomicCAS(status, 0, kStatusProbeWait);
 }
 
 // kNH (e4m3 only): 8-head tiles per kv head, ceil(g / 8)
@@ -1080,6 +1098,13 @@ int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pa
     if (rc != BSP_OK) return rc;
     return plan->group <= 8 ? launch_decode_bf16<128, true, true, 1>(tk, tv, p, grid, stream)
                             : launch_decode_bf16<128, true, true, 2>(tk, tv, p, grid, stream);
+}
+
+int launch_wait_probe(long long limit_cycles, int *status, cudaStream_t stream) {
+    wait_probe_kernel<<<1, 32, 0, stream>>>(limit_cycles, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("wait probe launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
 }
 
 int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace, cudaStream_t stream) {

@@ -358,6 +358,15 @@ int bsp_decode_run_static(const bsp_plan_info *plan, const void *host_staging, c
                           const void *k_pages, const void *v_pages, const int32_t *kv_indices,
                           float sm_scale, void *o, float *lse, bsp_stream_t stream);
 
+/* Self-test of the bounded waits every kernel uses: one warp waits on an
+ * mbarrier that nothing arrives at, with the kernels' spin (polls, and every
+ * 256 polls a clock and abort-flag check) and a limit of limit_cycles SM clock
+ * cycles (1 .. 2^33, about 4 s); when it gives up it writes 0x1ff into *status (device
+ * int32, set to 0 by the caller first) with the same compare-and-swap the
+ * kernels use on the workspace status word, and the kernel returns: no fault,
+ * the context stays usable. Stream-ordered; BSP_OK once launched. */
+int bsp_check_bounded_wait(int64_t limit_cycles, int32_t *status, bsp_stream_t stream);
+
 /* Read (and clear) the device error word that kernels set when a bounded wait
  * gives up or a bounds check trips (it lives in the workspace section at
  * plan->off_status). Synchronises `stream`. *word_out = 0 when clean;

@@ -88,3 +88,12 @@ def test_product_package_has_no_oracle_imports():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
                 assert "attention.c" not in text and "liboracle" not in text, f
+
+
+def test_bounded_wait_self_test_rejects_bad_arguments(native):
+    """Argument checks of bsp_check_bounded_wait happen on the host, before any
+    launch (no device needed)."""
+    lib = native.load()
+    assert lib.bsp_check_bounded_wait(1000, None, None) == native.BSP_ERR_INVALID_ARG
+    assert lib.bsp_check_bounded_wait(0, ctypes.c_void_p(16), None) == native.BSP_ERR_INVALID_ARG
+    assert lib.bsp_check_bounded_wait(1 << 34, ctypes.c_void_p(16), None) == native.BSP_ERR_INVALID_ARG

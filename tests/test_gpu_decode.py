@@ -220,3 +220,26 @@ def test_fused_merge_repeated_runs(bsp):
     torch.cuda.synchronize()
     assert torch.equal(o3, out) and torch.equal(l3, lse)
     assert pa.check_device_error() == 0
+
+
+def test_bounded_wait_gives_up(bsp):
+    """A wait that nothing completes (the kernels' bounded spin on an mbarrier
+    with no arrival) gives up after its limit and records its code in the status
+    word, without faulting: the context stays usable and a decode run right
+    after it is correct."""
+    import time
+    from block_sparse_paged_gb300 import _native as N
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    N.check(N.load().bsp_check_bounded_wait(4_000_000, ctypes.c_void_p(status.data_ptr()),
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == 0x1FF
+    assert elapsed < 2.0  # about 2 ms of SM clock, plus launch
+    b = workloads.paged_batch(91, [1] * 3, [300, 17, 900], 32, 8, 128, 16, "bf16", extra_pages=2)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=9)
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
