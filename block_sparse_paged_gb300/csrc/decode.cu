@@ -11,8 +11,8 @@
 //     table (sparse gather, dense compute: overview ⑥, walkthrough §IV.2 and
 //     §V.4). Pages of 8 or more tokens: one TMA tensor copy per page box
 //     (up to 64 rows of one kv head, 128-byte swizzle), page ids read 32 boxes
-//     at a time one batch ahead; 3 stages of 128 tokens. Smaller pages: 16-byte
-//     cp.async copies into padded rows, 2 stages of 128 tokens. Stages are large
+//     at a time one batch ahead. Smaller pages: 16-byte cp.async copies into the
+//     same swizzled layout. 3 stages of 128 tokens either way. Stages are large
 //     because each carries a fixed handshake cost. mbarriers carry the
 //     handshake (full: the stage's bytes / every lane's copies landed; empty:
 //     the compute warps are done with it); the ring runs across the CTA's work
@@ -89,33 +89,32 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// kTma: K and V arrive by TMA tensor copies, one per page box, as 128-byte
-// swizzled [D / 64][64 rows][128 B] tiles; otherwise by 16-byte cp.async into
-// padded rows.
+// kTma: K and V arrive by TMA tensor copies, one per page box; otherwise by
+// 16-byte cp.async; both into 128-byte swizzled [D / 64][rows][128 B] tiles.
 // kFp8 (with kTma, D = 128): the ring holds e4m3 rows (128 bytes, one swizzle
 // row); the compute warps read the bytes straight into f16 tensor-core
 // fragments (no staging copy).
 template <int D, bool kTma, bool kFp8 = false, int kNH = 1>
 struct DecodeLayout {
-    // kFp8: 128-token stages (half the bytes per token, so the same bytes per
-    // stage and per barrier round trip) shared by 8 compute warps, two per
-    // scheduler, so that each hides the other's latency
-    // bf16: 128-token stages too, each of the 4 compute warps taking two
-    // 16-token sub-blocks per stage: 3 stages of 64 KB with TMA, 2 of 68 KB
-    // (padded rows) with cp.async. Fewer, larger stages: a stage's fixed
+    // bf16: 3 stages of 128 tokens (64 KB), each of the 4 compute warps taking
+    // two 16-token sub-blocks per stage. Fewer, larger stages: a stage's fixed
     // handshake cost is spread over more bytes.
-    // e4m3 with g <= 8: 256-token stages (64 KB), 3 of them, two sub-blocks per
-    // warp (the head-major scratch needs only 8 rows per warp then).
+    // e4m3 with g <= 8: 256-token stages (64 KB), 3 of them, 8 compute warps (two
+    // per scheduler, each hiding the other's latency) taking two sub-blocks
+    // each (the head-major scratch needs only 8 rows per warp then); g > 8:
+    // 128-token stages, 5 of them.
     static constexpr int kTK = kFp8 ? (kNH == 1 ? 4 * kTileK : 2 * kTileK) : 2 * kTileK;
-    static constexpr int kS = kTma ? ((kFp8 && kNH == 2) ? kStages : 3) : 2;  // ring stages
+    static constexpr int kS = (kFp8 && kNH == 2) ? kStages : 3;  // ring stages
     static constexpr int kCons = kFp8 ? 8 : 4;                               // compute warps
     static constexpr int kSubB = kTK / (16 * kCons);                         // 16-token sub-blocks per warp and stage
     static constexpr int kScrRows = kFp8 ? 8 * kNH : kMmaRows;               // scratch rows per warp
     static constexpr int kThreads = 32 * (kCons + 2);
     static constexpr int kElem = kFp8 ? 1 : 2;               // bytes per K/V element in the ring
-    static constexpr int kPitch = kTma ? 128 : D * 2 + 16;  // row pitch inside a 128-byte-wide slab
-    static constexpr int kSlab = kTma ? kTK * 128 : 0;      // bytes per 128-byte-wide slab (TMA layout)
-    static constexpr int kTileBytes = kTma ? kTK * D * kElem : kTK * kPitch;  // K (or V) part of a stage
+    // Both gathers fill the same layout: [D * elem / 128 slabs][kTK rows][128 B],
+    // 16-byte chunks XOR-swizzled by row (TMA's 128-byte swizzle; the cp.async
+    // gather writes the same addresses), so rows need no padding.
+    static constexpr int kSlab = kTK * 128;                  // bytes per 128-byte-wide slab
+    static constexpr int kTileBytes = kTK * D * kElem;      // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kS * kStageBytes;
     static constexpr int kScratchOff = kRingBytes;
@@ -127,8 +126,7 @@ struct DecodeLayout {
     static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
     // byte offset of 16-byte chunk c (of D / 8) of ring row r inside a K or V tile
     __device__ static __forceinline__ uint32_t chunk(int r, int c) {
-        if constexpr (kTma) return (uint32_t)((c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-        else return (uint32_t)(r * kPitch + c * 16);
+        return (uint32_t)((c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4));
     }
 };
 
@@ -376,13 +374,13 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                                               kStatusProducerWait);
                 if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: every lane leaves together
                 const int n = min(kTK, len - t * kTK);
-                const uint32_t dst = sbase + s * LY::kStageBytes + part + (uint32_t)my_chunk * 16;
+                const uint32_t dst = sbase + s * LY::kStageBytes + part;
 #pragma unroll
                 for (int i = 0; i < kTK / T; ++i) {
                     const int j = i * T + my_sub;                     // token within the stage
                     const int half = (i * T) >> 5;                    // same for the whole warp: T divides 32
                     const uint64_t o = __shfl_sync(0xffffffffu, off[half], j & 31);
-                    if (j < n) cp_async_16(dst + j * LY::kPitch, src + o + my_chunk * 16, 16);
+                    if (j < n) cp_async_16(dst + LY::chunk(j, my_chunk), src + o + my_chunk * 16, 16);
                 }
                 // arrive on full[s] once this lane's copies have landed
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(full0 + 8 * s) : "memory");
