@@ -397,8 +397,13 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     float *stats = reinterpret_cast<float *>(smem + LY::kScratchOff + LY::kScratchBytes);  // [warp][16][m, l]
     int k = 0, merges = 0, lasts = 0;
     bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
+    bsp_work_item w_next = items[it0];
     for (int it = it0; it < it1; ++it) {
-        const bsp_work_item w = items[it];
+        // the next item is read at the start of this one, and its query rows are
+        // prefetched into L1 before this one's epilogue: neither load then sits
+        // at the next item's start
+        const bsp_work_item w = w_next;
+        if (it + 1 < it1) w_next = items[it + 1];
         const int len = w.kv_end - w.kv_start;
         const int nt = (len + kTK - 1) / kTK;
 
@@ -731,6 +736,11 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 *reinterpret_cast<float2 *>(scratch + (warp * kSR + r0) * D + col) = make_float2(acc[n][0], acc[n][1]);
                 *reinterpret_cast<float2 *>(scratch + (warp * kSR + r1) * D + col) = make_float2(acc[n][2], acc[n][3]);
             }
+        }
+        if (warp == 0 && it + 1 < it1 && lane * 128 < g * D * 2) {  // the next item's g query rows
+            const char *qn = static_cast<const char *>(p.q) +
+                             ((size_t)w_next.q_tok0 * p.H_qo + (size_t)w_next.kv_head * g) * D * 2 + lane * 128;
+            asm volatile("prefetch.global.L1 [%0];\n" ::"l"(qn));
         }
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(merge_in);
