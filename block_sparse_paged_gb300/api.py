@@ -121,8 +121,18 @@ class PagedAttention:
         self.info = None
 
     # ---- plan ---------------------------------------------------------------
-    def plan(self, kv_indptr, last_page_len, qo_indptr=None, alpha: int = 2, beta: int = 1, stream=None):
-        """Host plan from the request lengths; its copy is queued on `stream`."""
+    # Default per-position cost alpha of the LPT plan (cost of a work item =
+    # alpha * query positions + beta * KV tokens). The pages' constants are
+    # alpha = 2, beta = 1; a decode work item (one position) costs more than 2
+    # tokens of KV on this GPU: about 64 (its setup and epilogue, measured as the
+    # alpha that balanced a batch of short requests best: 59.0 -> 55.5 us).
+    DEFAULT_ALPHA = {N.BSP_MODE_DECODE: 64, N.BSP_MODE_PREFILL: 2}
+
+    def plan(self, kv_indptr, last_page_len, qo_indptr=None, alpha: int | None = None, beta: int = 1, stream=None):
+        """Host plan from the request lengths; its copy is queued on `stream`.
+        alpha defaults to DEFAULT_ALPHA[mode]."""
+        if alpha is None:
+            alpha = self.DEFAULT_ALPHA[self.mode]
         if self._copied is not None:
             self._copied.synchronize()  # the staging buffer is still the source of the previous copy
         kv = _i32_host(kv_indptr)
