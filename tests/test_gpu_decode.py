@@ -38,6 +38,9 @@ CASES = [
     (5, [100, 257, 0, 63], 4, 2, 64, 4, 6),
     (6, [2048, 1024, 17], 32, 4, 64, 1, 400),
     (7, [12345, 5, 999], 32, 8, 128, 32, 2),
+    (8, [513, 31, 64, 2000], 32, 2, 64, 8, 13),        # g = 16, D = 64, 8-row page boxes
+    (9, [129, 4000, 1], 32, 8, 128, 64, 9),            # 64-token pages: one box per stage half
+    (10, [300, 5000, 260, 17], 64, 8, 128, 256, 21),   # 256-token pages: four boxes per page
 ]
 
 
