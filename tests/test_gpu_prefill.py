@@ -30,6 +30,8 @@ CASES = [
     (8, [65, 300, 17], [65, 300, 17], 32, 8, 1, True, 11),              # page size 1: cp.async gather
     (9, [140, 33], [400, 33], 16, 4, 4, True, 6),                        # page size 4: cp.async gather
     (10, [96, 250], [96, 700], 32, 8, 32, False, 5),                     # page 32 (two pages per box row set)
+    (13, [150, 300], [400, 300], 32, 8, 64, True, 9),                    # 64-token pages
+    (14, [77, 260], [1000, 260], 16, 4, 256, True, 11),                  # 256-token pages: a page spans two KV tiles
 ]
 
 
