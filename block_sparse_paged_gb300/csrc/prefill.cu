@@ -437,9 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool full = valid == kKvTile && tok0 + kKvTile - 1 <= lim && tok0 >= lo;
                 if (!full) {
+                    // visible columns of this row: [c_lo, c_hi)
+                    const int c_hi = min(valid, lim == INT_MAX ? kKvTile : max(0, min(kKvTile, lim - tok0 + 1)));
+                    const int c_lo = kVar && lo != INT_MIN ? max(0, lo - tok0) : 0;
+                    if (kVar) {
 #pragma unroll
-                    for (int c = 0; c < kKvTile; ++c)
-                        sv[c] = (c < valid && tok0 + c <= lim && tok0 + c >= lo) ? sv[c] : -INFINITY;
+                        for (int c = 0; c < kKvTile; ++c)
+                            sv[c] = (unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) ? sv[c] : -INFINITY;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kKvTile; ++c) sv[c] = c < c_hi ? sv[c] : -INFINITY;
+                    }
                 }
                 // row maximum: 8 independent chains of 3-input maxima
                 float pm[8];
