@@ -43,7 +43,8 @@ class Problem(ctypes.Structure):
 
 
 class Capacity(ctypes.Structure):
-    _fields_ = [("max_batch", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("max_qo_tokens", ctypes.c_int64)]
+    _fields_ = [("max_batch", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("max_qo_tokens", ctypes.c_int64),
+                ("chunks_per_cta", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):

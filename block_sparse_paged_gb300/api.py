@@ -97,7 +97,7 @@ class PagedAttention:
     def __init__(self, mode: str, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  causal: bool = False, dtype=torch.bfloat16, max_batch: int = 256,
                  max_qo_tokens: int | None = None, num_ctas: int | None = None, device=None,
-                 window_left: int = -1, logits_soft_cap: float = 0.0):
+                 window_left: int = -1, logits_soft_cap: float = 0.0, chunks_per_cta: int = 1):
         self.lib = N.load()
         if mode not in ("decode", "prefill"):
             raise ValueError("mode must be 'decode' or 'prefill'")
@@ -110,7 +110,7 @@ class PagedAttention:
             num_ctas = default_num_ctas(self.mode, self.device.index)
         if max_qo_tokens is None:
             max_qo_tokens = max_batch if mode == "decode" else 65536
-        self.capacity = N.Capacity(max_batch, num_ctas, max_qo_tokens)
+        self.capacity = N.Capacity(max_batch, num_ctas, max_qo_tokens, chunks_per_cta)
         ws_bytes = self.lib.bsp_workspace_size(ctypes.byref(self.problem), ctypes.byref(self.capacity))
         st_bytes = self.lib.bsp_host_staging_size(ctypes.byref(self.problem), ctypes.byref(self.capacity))
         if ws_bytes == 0 or st_bytes == 0:

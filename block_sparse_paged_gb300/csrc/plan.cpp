@@ -39,10 +39,16 @@ bool check_problem(const bsp_problem *p) {
     return true;
 }
 
+// s of L = ceil(W / (s C)); a zero-initialised capacity plans with s = 1
+static int chunks_per_cta(const bsp_capacity *c) { return c->chunks_per_cta > 0 ? c->chunks_per_cta : 1; }
+
 bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
     if (!check_problem(p)) return false;
     if (!c || c->max_batch < 0 || c->num_ctas < 1 || c->max_qo_tokens < 0)
         return fail(BSP_ERR_INVALID_ARG, "capacity needs max_batch >= 0, num_ctas >= 1, max_qo_tokens >= 0"), false;
+    if (c->chunks_per_cta < 0 || c->chunks_per_cta > 64)
+        return fail(BSP_ERR_INVALID_ARG, "capacity.chunks_per_cta must be in [0, 64]"), false;
+    const int64_t sC = (int64_t)chunks_per_cta(c) * c->num_ctas;
     const int g = p->num_qo_heads / p->num_kv_heads;
     Layout l;
     l.group = g;
@@ -53,11 +59,11 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
         ? c->max_qo_tokens
         : (c->max_qo_tokens * g + kPrefillTileRows - 1) / kPrefillTileRows + c->max_batch;
     l.cap_tiles = tiles_per_head * p->num_kv_heads;
-    // Chunks: each tile has max(1, ceil(v / L)) <= 1 + v / L and sum v / L <= W / L <= C.
-    l.cap_items = l.cap_tiles + c->num_ctas;
-    // Split tiles: v > L gives ceil(v / L) <= 2 v / L slots, summing to <= 2 C.
-    l.cap_partials = 2 * (int64_t)c->num_ctas;
-    l.cap_merges = std::min<int64_t>(l.cap_tiles, c->num_ctas);
+    // Chunks: each tile has max(1, ceil(v / L)) <= 1 + v / L and sum v / L <= W / L <= s C.
+    l.cap_items = l.cap_tiles + sC;
+    // Split tiles: v > L gives ceil(v / L) <= 2 v / L slots, summing to <= 2 s C.
+    l.cap_partials = 2 * sC;
+    l.cap_merges = std::min<int64_t>(l.cap_tiles, sC);
     if (l.cap_items > INT32_MAX / 2) return fail(BSP_ERR_CAPACITY, "capacity too large"), false;
 
     uint64_t off = 0;
@@ -157,8 +163,9 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
         W += (packed + T - 1) / T * kv_len_of(kv_indptr_h, last_page_len_h, P.page_size, b) * H;
     }
 
-    // ---- 3: chunk length L = ceil(W / C), rounded up to whole pages --------
-    int64_t Lc = std::max<int64_t>(1, (W + C - 1) / C);
+    // ---- 3: chunk length L = ceil(W / (s C)), rounded up to whole pages ----
+    const int64_t sC = (int64_t)chunks_per_cta(capacity) * C;
+    int64_t Lc = std::max<int64_t>(1, (W + sC - 1) / sC);
     Lc = (Lc + P.page_size - 1) / P.page_size * P.page_size;
     Lc = std::min<int64_t>(Lc, (int64_t)INT32_MAX / 2 / P.page_size * P.page_size);
 

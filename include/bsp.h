@@ -120,6 +120,12 @@ typedef struct bsp_capacity {
                                queues, so C = R + 1 .. 2R - 1 leaves SMs idle:
                                prefer R (bsp_default_num_ctas) or a multiple  */
     int64_t max_qo_tokens;  /* total query positions per plan                     */
+    int32_t chunks_per_cta; /* s >= 1 (0 reads as 1): the chunk length becomes
+                               L = ceil(W / (s C)), about s chunks per queue, so
+                               that LPT can even out batches of few, equal tiles
+                               (s = 1 is the pages' L = ceil(W / C)). Bounds the
+                               work items by tiles + s C and the partial slots
+                               by 2 s C; at most 64                            */
 } bsp_capacity;
 
 /* One work item of the plan (64 bytes, device and staging image). */
@@ -182,7 +188,7 @@ typedef struct bsp_plan_info {
 int bsp_default_num_ctas(int32_t mode, int32_t device, int32_t *num_ctas_out);
 
 /* Bytes of device workspace for these bounds: plan metadata plus partial
- * states. Partial slots are bounded by 2 C (technical review §6.5 eq 13, per
+ * states. Partial slots are bounded by 2 s C (technical review §6.5 eq 13, per
  * query tile and kv head). Returns 0 on invalid input. */
 size_t bsp_workspace_size(const bsp_problem *problem, const bsp_capacity *capacity);
 
@@ -194,7 +200,7 @@ size_t bsp_host_staging_size(const bsp_problem *problem, const bsp_capacity *cap
  * Algorithm 2; engineering walkthrough §VIII.2, §VIII.5):
  *   query tiles of T_q packed rows (decode: g rows, one position; prefill:
  *   256 rows), W = sum over (tile, kv head) of kv_len, chunk length
- *   L = ceil(W / C) rounded up to a page, chunks of each tile's visible range
+ *   L = ceil(W / (s C)) rounded up to a page (s = capacity->chunks_per_cta), chunks of each tile's visible range
  *   sorted longest first (ties by (b, tile, kv_head, kv_start)), assigned to
  *   CTAs by a min-heap on (cost, cta), cost += alpha * positions + beta *
  *   chunk tokens; outputs with one chunk are written through, the others get

@@ -18,7 +18,9 @@ Attention Engine, §VIII.2 and §VIII.5):
    kv head is an axis of the work items).
 3. L = max(1, ceil(W / C)) (Algorithm 2 step 4 and the overview's worked
    example use the ceiling), then rounded up to a multiple of the page size so
-   that no chunk splits a page.
+   that no chunk splits a page. An optional s = chunks_per_cta > 1 (not on
+   the pages; this build's extension) takes L = ceil(W / (s C)) instead, about
+   s chunks per CTA, so that LPT can even out batches of few, equal tiles.
 4. Each output tile's visible KV range [lo, v) is cut into chunks of at most
    L tokens from lo on (Algorithm 2 step 5). Non-causal: v = kv_len. Causal
    with bottom-right alignment: v = min(kv_len, last_pos + kv_len - qo_len + 1)
@@ -104,7 +106,7 @@ def visible_len(qo_len: int, kv_len: int, last_pos: int, causal: bool) -> int:
 
 def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
          num_ctas: int, page_size: int, causal: bool, alpha: int = 2, beta: int = 1,
-         window_left: int = -1) -> Plan:
+         window_left: int = -1, chunks_per_cta: int = 1) -> Plan:
     if tile_rows % group != 0:
         raise ValueError("tile_rows must be a multiple of the group size")
     if num_ctas < 1 or page_size < 1:
@@ -127,8 +129,9 @@ def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
                 tiles.append((b, t, h, p1 - p0, lo, vis))
                 W += kv_lens[b]
 
-    # 3: chunk length
-    L = max(1, -(-W // num_ctas))
+    # 3: chunk length; s = chunks_per_cta > 1 divides it further (s = 1 is the
+    # pages' L = ceil(W / C))
+    L = max(1, -(-W // (num_ctas * max(1, chunks_per_cta))))
     L = -(-L // page_size) * page_size
 
     # 4: chunks per output tile, partial slots and the reduction map

@@ -41,6 +41,9 @@ CASES = [
     (8, [513, 31, 64, 2000], 32, 2, 64, 8, 13),        # g = 16, D = 64, 8-row page boxes
     (9, [129, 4000, 1], 32, 8, 128, 64, 9),            # 64-token pages: one box per stage half
     (10, [300, 5000, 260, 17], 64, 8, 128, 256, 21),   # 256-token pages: four boxes per page
+    (11, [4096, 130, 3, 1, 700], 64, 8, 128, 1, 19),   # page 1, g = 8, ragged stage tails
+    (12, [1000, 37, 2500, 6], 32, 8, 128, 12, 9),      # 12-token pages (not a power of two): cp.async
+    (13, [513, 2, 3001], 8, 2, 64, 2, 7),              # D = 64, 2-token pages
 ]
 
 
@@ -79,6 +82,32 @@ def test_vector_sparse_permuted_equals_contiguous(bsp):
     tok, head = sample_rows(perm, 128, 12)
     O, L = oracle.attention_rows_of(perm, tok, head)
     compare(out_p, lse_p, O, L, "bf16", rows=(tok, head))
+
+
+@pytest.mark.parametrize("ps,D", [(16, 128), (8, 64), (64, 128)])
+def test_tma_gather_equals_cp_async_gather(bsp, ps, D):
+    """Pages of 8 or more tokens are gathered by TMA page boxes when the pool
+    size is known, by 16-byte cp.async copies when it is not (num_pages 0):
+    the two loaders fill the same swizzled tiles, so the outputs are bitwise
+    equal; both match the oracle."""
+    import ctypes
+    b = workloads.paged_batch(50 + ps, np.ones(5, int), [3001, 17, 1, 640, 129], 32, 8, D, ps, "bf16",
+                              extra_pages=3)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=23)
+    compare(out, lse, O, L, "bf16")
+    q, k, v, idx = to_dev(b)
+    out0 = torch.empty_like(q)
+    lse0 = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    rc = pa.lib.bsp_decode_run(ctypes.byref(pa.info), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                               ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(idx.data_ptr()), 0,
+                               ctypes.c_float(b.sm_scale), ctypes.c_void_p(out0.data_ptr()),
+                               ctypes.c_void_p(lse0.data_ptr()), ctypes.c_void_p(pa.workspace.data_ptr()),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert pa.check_device_error() == 0
+    assert torch.equal(out.cuda(), out0) and torch.equal(lse.cuda(), lse0)
 
 
 def test_shared_prefix_full_view_decode(bsp):

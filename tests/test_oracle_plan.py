@@ -147,6 +147,21 @@ def pin_empty_tiles(pl):
     assert sorted((it.b, it.kv_head, it.kv_start, it.kv_end) for it in items if it.b == 0) == [(0, 0, 0, 0), (0, 1, 0, 0)]
 
 
+def pin_chunks_per_cta(pl):
+    """s chunks per CTA: L = ceil(W / (s C)). Two 4096-token tiles on 2 CTAs
+    with s = 4 give L = 1024, four equal chunks per tile and four chunks (4096
+    tokens plus alpha per chunk) per CTA; s = 1 (and 0, read as 1) keeps the
+    pages' L = ceil(W / C) = 4096, one chunk per tile."""
+    p = pl.plan([1, 1], [4096, 4096], 1, 1, 1, 2, 1, False, alpha=2, beta=1, chunks_per_cta=4)
+    assert p.chunk_len == 1024 and p.num_partials == 8
+    assert sorted(len(q) for q in p.queues) == [4, 4] and p.cta_cost == [4096 + 8, 4096 + 8]
+    for s in (0, 1):
+        p1 = pl.plan([1, 1], [4096, 4096], 1, 1, 1, 2, 1, False, chunks_per_cta=s)
+        assert p1.chunk_len == 4096 and p1.num_partials == 0
+    p3 = pl.plan([1], [1000], 1, 1, 1, 1, 16, False, chunks_per_cta=3)  # ceil(1000 / 3) = 334 -> 336 (pages)
+    assert p3.chunk_len == 336 and [(it.kv_start, it.kv_end) for it in p3.queues[0]] == [(0, 336), (336, 672), (672, 1000)]
+
+
 def pin_traffic_ratio(pl):
     """Technical review eq 15 limits: n = 1 gives 1; no suffix gives n."""
     assert pl.prefix_traffic_ratio(1, 8192, 300) == pytest.approx(1.0)
@@ -154,7 +169,7 @@ def pin_traffic_ratio(pl):
 
 
 ALL_PLAN_PINS = [pin_lpt_worked_example, pin_capacity_formula, pin_coverage, pin_chunk_len_and_bounds,
-                 pin_lpt_quality, pin_determinism, pin_empty_tiles, pin_traffic_ratio]
+                 pin_lpt_quality, pin_determinism, pin_empty_tiles, pin_chunks_per_cta, pin_traffic_ratio]
 
 
 @pytest.mark.parametrize("pin", ALL_PLAN_PINS, ids=lambda f: f.__name__)
@@ -163,7 +178,10 @@ def test_plan_pin(pin):
 
 
 PLAN_MUTATIONS = [
-    ("floor_chunk", "L = max(1, -(-W // num_ctas))", "L = max(1, W // num_ctas)"),
+    ("floor_chunk", "L = max(1, -(-W // (num_ctas * max(1, chunks_per_cta))))",
+     "L = max(1, W // (num_ctas * max(1, chunks_per_cta)))"),
+    ("chunks_per_cta_ignored", "L = max(1, -(-W // (num_ctas * max(1, chunks_per_cta))))",
+     "L = max(1, -(-W // num_ctas))"),
     ("no_page_rounding", "L = -(-L // page_size) * page_size", "L = L"),
     ("shortest_first", "chunks.sort(key=lambda c: (-(c[4] - c[3]), c[0], c[1], c[2], c[3]))",
      "chunks.sort(key=lambda c: ((c[4] - c[3]), c[0], c[1], c[2], c[3]))"),

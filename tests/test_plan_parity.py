@@ -16,7 +16,7 @@ def bsp():
 
 
 def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alpha=2, beta=1, D=128,
-             max_batch=None, max_qo=None, window_left=-1):
+             max_batch=None, max_qo=None, window_left=-1, s=1):
     qo_lens = np.asarray(qo_lens, np.int64)
     kv_lens = np.asarray(kv_lens, np.int64)
     B = len(kv_lens)
@@ -29,13 +29,13 @@ def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alph
     g = H_qo // H_kv
     prob = bsp.make_problem(mode, H_qo, H_kv, D, page_size, causal, __import__("torch").bfloat16,
                             window_left=window_left)
-    cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]))
+    cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]), s)
     info, queue, items, merges = bsp.plan_host(prob, cap, kv_indptr, last,
                                                None if mode == bsp.BSP_MODE_DECODE and np.all(qo_lens == 1) else qo_indptr,
                                                alpha, beta)
     tile = g if mode == bsp.BSP_MODE_DECODE else 256
     ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta,
-                     window_left=window_left)
+                     window_left=window_left, chunks_per_cta=s)
     return info, queue, items, merges, ref, qo_indptr, kv_indptr
 
 
@@ -92,6 +92,42 @@ def test_random_decode_and_prefill(bsp, seed):
     assert_same(*out)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_plans_with_chunks_per_cta(bsp, seed):
+    # s > 1: L = ceil(W / (s C)); the capacity bounds (tiles + s C items, 2 s C
+    # partial slots) must hold for every s, so the random cases reach s = 64
+    rng = np.random.default_rng(5000 + seed)
+    B = int(rng.integers(1, 40))
+    H_kv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 4, 8]))
+    ps = int(rng.choice([1, 3, 16]))
+    C = int(rng.integers(1, 200))
+    s = int(rng.choice([2, 4, 7, 64]))
+    kv = rng.integers(0, 5000, size=B)
+    if seed % 2 == 0:
+        out = run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(B, int), kv, ps, H_kv * g, H_kv, False, C, alpha=64, s=s)
+    else:
+        qo = np.maximum(1, np.minimum(kv, rng.integers(1, 700, size=B)))
+        out = run_both(bsp, bsp.BSP_MODE_PREFILL, qo, kv, ps, H_kv * g, H_kv, True, C, s=s)
+    assert_same(*out)
+    info, queue = out[0], out[1]
+    assert info.num_items <= info.cap_items and info.num_partials <= info.cap_partials
+
+
+def test_vector_sparse_decode_balance_with_chunks_per_cta(bsp):
+    # 32 requests x 4096 tokens x 8 kv heads on 152 queues: with s = 1 no tile is
+    # split (L = 6899) and 104 queues carry two tiles while 48 carry one; s = 4
+    # splits every tile so that the busiest queue carries at most 0.92 / 0.83 of
+    # the s = 1 load
+    loads = {}
+    for s in (1, 4):
+        out = run_both(bsp, bsp.BSP_MODE_DECODE, [1] * 32, [4096] * 32, 1, 64, 8, False, 152, alpha=64, s=s)
+        assert_same(*out)
+        loads[s] = max(out[4].cta_cost)
+    ideal = 32 * 4096 * 8 / 152
+    assert ideal / loads[1] < 0.84 and ideal / loads[4] > 0.91
+
+
 def test_benchmark_workload_lengths(bsp):
     b2 = workloads.batched_decode_bf16()
     assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, b2.qo_lens, b2.kv_lens, 16, 32, 8, False, 304))
@@ -109,6 +145,10 @@ def test_capacity_and_metadata_errors(bsp):
         bsp.plan_host(prob, bsp.Capacity(2, 8, 2), [0, 1, 2, 3], [1, 1, 1])          # batch 3 > 2
     with pytest.raises(bsp.BspError, match="INVALID_ARG"):
         bsp.plan_host(prob, bsp.Capacity(4, 8, 4), [0, 2, 1], [1, 1])                # indptr decreasing
+    with pytest.raises(bsp.BspError, match="INVALID_ARG"):
+        bsp.plan_host(prob, bsp.Capacity(4, 8, 4, 65), [0, 1, 2], [1, 1])            # chunks_per_cta > 64
+    with pytest.raises(bsp.BspError, match="INVALID_ARG"):
+        bsp.plan_host(prob, bsp.Capacity(4, 8, 4, -1), [0, 1, 2], [1, 1])
     with pytest.raises(bsp.BspError, match="INVALID_ARG"):
         bsp.plan_host(prob, bsp.Capacity(4, 8, 4), [0, 2, 3], [1, 5])                # last_page_len > page
     with pytest.raises(bsp.BspError, match="INVALID_ARG"):
