@@ -442,14 +442,20 @@ def secondary(bsp, dev, args, pk):
         C = args.num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
         pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, 1, False, torch.bfloat16,
                                 max_batch=b.batch, num_ctas=C, device=dev)
-        attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm)
-        gbs = decode_bytes(b) / ((attn + merge) * 1e-3) / 1e9
-        r[tag] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "attn_ms": round(attn, 4),
-                  "merge_ms": round(merge, 4)}
-        del pa
+        pa.plan(b.kv_indptr, b.last_page_len)
+        q, k, v, idx = to_dev(b, dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        st = torch.cuda.Stream(device=dev)
+        # one launch per run (split outputs are merged inside the kernel)
+        ms = graph_time(lambda: pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, stream=st), st, steps, warm)
+        gbs = decode_bytes(b) / (ms * 1e-3) / 1e9
+        r[tag] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4)}
+        del pa, q, k, v, out, lse
         torch.cuda.empty_cache()
     r["permuted_over_contiguous"] = round(r["permuted"]["GB/s"] / r["contiguous"]["GB/s"], 4)
-    r["workload"] = "32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16"
+    r["workload"] = ("32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16; "
+                     "one launch per run, 10 per graph replay")
     res["vector_sparse_decode"] = r
     del perm, cont
     res["ragged_causal_prefill"] = ragged_prefill(bsp, dev, steps, warm, pk)
@@ -492,6 +498,31 @@ def ragged_prefill(bsp, dev, steps, warm, pk):
                      "algorithmic_flops_per_launch": fl}}
 
 
+def graph_time(run, st, steps, warm, reps=10):
+    """Mean time (ms) of one run() call, launched `reps` times per CUDA graph
+    replay so that the host's per-call cost stays out of the kernel time."""
+    with torch.cuda.stream(st):
+        for _ in range(warm):
+            run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for _ in range(reps):
+            run()
+    graph.replay()
+    n_rep = max(1, steps // reps)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()  # replay() launches on the current stream
+    for i in range(n_rep):
+        graph.replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(n_rep)) / reps
+    del graph
+    return ms
+
+
 def fp8_decode(bsp, dev, steps, warm, pk):
     """The batched decode workload with e4m3 K / V pools (one scale each):
     algorithmic bytes as for bf16 but one byte per K / V element."""
@@ -511,30 +542,11 @@ def fp8_decode(bsp, dev, steps, warm, pk):
 
     def run():
         pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, k_scale=f8.k_scale, v_scale=f8.v_scale, stream=st)
-    # 10 launches per CUDA graph replay: the host's per-call cost stays out of the kernel time
-    reps = 10
-    with torch.cuda.stream(st):
-        for _ in range(warm):
-            run()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=st):
-        for _ in range(reps):
-            run()
-    graph.replay()
-    n_rep = max(1, steps // reps)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
-    torch.cuda.synchronize()
-    ev[0].record()  # replay() launches on the current stream
-    for i in range(n_rep):
-        graph.replay()
-        ev[i + 1].record()
-    torch.cuda.synchronize()
-    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(n_rep)) / reps
+    ms = graph_time(run, st, steps, warm)
     kv_tokens = int(b.kv_lens.sum())
     nbytes = decode_bytes(b) - kv_tokens * b.num_kv_heads * b.head_dim * 2 * (esize(b) - 1)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    del graph, pa, q, k, v
+    del pa, q, k, v
     torch.cuda.empty_cache()
     return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
             "bytes": nbytes, "tokens_per_s": round(b.batch / (ms * 1e-3), 1),

@@ -149,39 +149,54 @@ struct DecodeParams {
     const float *sink;       // per-qo-head sink logits, or null
 };
 
-// Merge of one reduction-map entry by warps w = 0..nwarps-1 of the CTA that
-// wrote its last partial state: the fold of its slots with one common maximum
-// (technical review §3.2 eq 6), final O and LSE written. One warp per output
-// row: lanes read the slots' LSEs side by side (32 at a time), the maximum and
-// the weights come by shuffle, and each lane folds its own D / 32 columns with
-// independent loads. The partials were written by other CTAs: read through L2.
+// Merge of one reduction-map entry by threads t = 0..nthreads-1 of the CTA that
+// wrote its last partial state: the fold of its slots (technical review §3.2
+// eq 6), final O and LSE written. The partials were written by other CTAs and
+// are read through L2, so the fold is latency-bound: each thread takes one
+// (row, 4 columns) unit and issues the loads of up to 8 slots (their LSEs and
+// float4 columns) before using any, one round trip per 8 slots instead of one
+// per slot. Up to 8 slots this is the fold with one common maximum; longer
+// entries fold 8 slots at a time, rescaling to the running maximum.
 template <int D, typename OutT>
-__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int w, int nwarps,
-                                            int lane) {
-    constexpr int E = D / 32;
+__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int t, int nthreads) {
+    constexpr int kQ = D / 4;     // column quads per row
+    constexpr int kBatch = 8;     // slots whose loads are in flight together
     const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
-    const float *po = reinterpret_cast<const float *>(p.ws + p.off_po);
+    const float4 *po = reinterpret_cast<const float4 *>(p.ws + p.off_po);
     const int rows = e.n_pos * p.g;
-    for (int r = w; r < rows; r += nwarps) {
-        float M = -INFINITY;
-        for (int s0 = 0; s0 < e.n_slots; s0 += 32)
-            if (s0 + lane < e.n_slots) M = fmaxf(M, __ldcg(plse + (size_t)(e.slot_begin + s0 + lane) * p.tile_rows + r));
+    for (int u = t; u < rows * kQ; u += nthreads) {
+        const int r = u / kQ, cq = u - r * kQ;
+        float M = -INFINITY, L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < e.n_slots; s0 += kBatch) {
+            const int ns = min(kBatch, e.n_slots - s0);
+            float l[kBatch];
+            float4 o[kBatch];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float acc[E], L = 0.f;
+            for (int j = 0; j < kBatch; ++j) {
+                const size_t prow = (size_t)(e.slot_begin + s0 + j) * p.tile_rows + r;
+                l[j] = j < ns ? __ldcg(plse + prow) : -INFINITY;
+                o[j] = j < ns ? __ldcg(po + prow * kQ + cq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float Mb = M;
 #pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] = 0.f;
-        if (M != -INFINITY) {
-            for (int s0 = 0; s0 < e.n_slots; s0 += 32) {
-                const int ns = min(32, e.n_slots - s0);
-                const size_t prow0 = (size_t)(e.slot_begin + s0) * p.tile_rows + r;
-                const float my_w = lane < ns ? exp2f((__ldcg(plse + prow0 + (size_t)lane * p.tile_rows) - M) * kLog2e) : 0.f;
-                for (int s = 0; s < ns; ++s) {
-                    const float wgt = __shfl_sync(0xffffffffu, my_w, s);
-                    const float *src = po + (prow0 + (size_t)s * p.tile_rows) * D + lane * E;
+            for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, l[j]);
+            if (Mb == -INFINITY) continue;  // every slot so far empty
+            if (M != Mb) {                   // rescale what was folded to the new maximum
+                const float f = M == -INFINITY ? 0.f : exp2f((M - Mb) * kLog2e);
+                L *= f;
+                acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+                M = Mb;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (j < ns) {
+                    const float wgt = exp2f((l[j] - M) * kLog2e);
                     L += wgt;
-#pragma unroll
-                    for (int i = 0; i < E; ++i) acc[i] = fmaf(wgt, __ldcg(src + i), acc[i]);
+                    acc.x = fmaf(wgt, o[j].x, acc.x);
+                    acc.y = fmaf(wgt, o[j].y, acc.y);
+                    acc.z = fmaf(wgt, o[j].z, acc.z);
+                    acc.w = fmaf(wgt, o[j].w, acc.w);
                 }
             }
         }
@@ -189,10 +204,12 @@ __device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_mer
         float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
         if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
         const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
-        OutT *dst = static_cast<OutT *>(p.o) + orow * D + lane * E;
-#pragma unroll
-        for (int i = 0; i < E; ++i) dst[i] = from_float<OutT>(acc[i] * inv);
-        if (lane == 0 && p.lse) p.lse[orow] = lse_row;
+        OutT *dst = static_cast<OutT *>(p.o) + orow * D + cq * 4;
+        dst[0] = from_float<OutT>(acc.x * inv);
+        dst[1] = from_float<OutT>(acc.y * inv);
+        dst[2] = from_float<OutT>(acc.z * inv);
+        dst[3] = from_float<OutT>(acc.w * inv);
+        if (cq == 0 && p.lse) p.lse[orow] = lse_row;
     }
 }
 
@@ -792,7 +809,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             if (*last_flag) {
                 __threadfence();
                 const bsp_merge_entry e = mmap[w.merge];
-                merge_entry<D, __nv_bfloat16>(p, e, warp, kConsumers, lane);
+                merge_entry<D, __nv_bfloat16>(p, e, warp * 32 + lane, kConsumers * 32);
                 if (warp == 0 && lane == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
             }
         }
@@ -866,7 +883,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_f32_kernel(const DecodePar
             if (s_last) {
                 __threadfence();
                 const bsp_merge_entry e = mmap[w.merge];
-                merge_entry<D, float>(p, e, threadIdx.x >> 5, kDecWarps, threadIdx.x & 31);
+                merge_entry<D, float>(p, e, threadIdx.x, kDecWarps * 32);
                 if (threadIdx.x == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
             }
             __syncthreads();
