@@ -603,12 +603,17 @@ def shared_prefix_bytes(sp) -> int:
     return sp.prefix_len * kvrow + int(sp.suffix_lens.sum()) * kvrow + qo + lse + meta
 
 
-def shared_prefix_split(bsp, dev):
-    """SMs for the prefix view (prefill kernel): a third of them (swept on this
-    workload: 0.12-0.33 of the SMs gave 95-90 us per step, a third the best);
-    the rest run the suffix view concurrently."""
+def shared_prefix_split(bsp, dev, prefix_tiles: int = 8):
+    """CTAs for the prefix view (prefill kernel); the rest run the suffix view
+    concurrently. A multiple of the prefix view's output tiles (8: one 256-row
+    tile per kv head) gives every CTA one equal chunk of the shared pages;
+    among those, the one nearest a fifth of the SMs. Swept on this workload
+    (GB300, 152 SMs): 16 / 24 / 32 / 40 / 48 CTAs 89.5 / 73.3 / 68.3 / 73.3 /
+    74.8 us per step; counts that split the chunks unevenly are slower (20:
+    86.4, 51: 77.6)."""
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return max(8, min(sms - 8, round(sms / 3))), sms
+    c = max(prefix_tiles, round(sms / 5 / prefix_tiles) * prefix_tiles)
+    return min(c, sms - 8), sms
 
 
 def shared_prefix(bsp, dev, steps, warm, pk):
