@@ -478,11 +478,16 @@ def secondary(bsp, dev, args, pk):
 
 
 def ragged_prefill(bsp, dev, steps, warm, pk):
-    """The ragged causal prefill workload, kernel-only timing with a roofline."""
+    """The ragged causal prefill workload, kernel-only timing with a roofline.
+    Planned for two LPT queues per CTA (each CTA runs two consecutive queues):
+    swept on GB300 (graph-timed, alpha 2), 152 / 304 / 456 queues 279.4 /
+    273.8 / 283.0 us; no tile is split at any of them."""
     import workloads
     b = workloads.ragged_causal_prefill_bf16()
+    C = 2 * torch.cuda.get_device_properties(dev).multi_processor_count
     pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
-                            torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+                            torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), num_ctas=C,
+                            device=dev)
     attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
     fl = prefill_flops(b)
     tf = fl / ((attn + merge) * 1e-3) / 1e12
@@ -490,7 +495,8 @@ def ragged_prefill(bsp, dev, steps, warm, pk):
     return {
         "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "flops": fl,
         "attn_ms": round(attn, 4), "merge_ms": round(merge, 4),
-        "workload": "16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, D 128, bf16, causal",
+        "workload": "16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, D 128, bf16, causal; "
+                    "plan of 2 queues per CTA", "plan_queues": C,
         "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(ka, 1),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ka / pk["bf16_tflops"], 4),
                      "peak_source": "measured (cuBLAS bf16 burst; the kernel is timed alone)",

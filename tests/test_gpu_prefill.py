@@ -135,6 +135,12 @@ def test_ragged_causal_prefill_full_size(bsp):
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
     assert pa.check_device_error() == 0
+    # the bench's plan: two queues per CTA. No tile is split under either plan,
+    # so every output row is computed the same way: bitwise equal
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out3, lse3, pa3 = run_batch(bsp, b, mode="prefill", num_ctas=2 * sms, dev_tensors=(q, k, v, idx))
+    assert pa3.info.num_merges == 0 and pa.info.num_merges == 0
+    assert torch.equal(out, out3) and torch.equal(lse, lse3)
 
 
 def composable_decode(bsp, sp, num_ctas_prefill=None, num_ctas_decode=None):
@@ -210,6 +216,11 @@ def test_shared_prefix_composable_full_size(bsp):
     tok, head = sample_rows(sp.full, 256, 22)
     O, L = oracle.attention_rows_of(sp.full, tok, head)
     compare(out, lse, O, L, "bf16", rows=(tok, head))
+    # the bench's split: 32 CTAs for the prefix view (4 equal chunks per tile),
+    # the rest for the suffix view
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out2, lse2 = composable_decode(bsp, sp, num_ctas_prefill=32, num_ctas_decode=sms - 32)
+    compare(out2, lse2, O, L, "bf16", rows=(tok, head))
 
 
 def test_vector_sparse_prefill_small(bsp):
