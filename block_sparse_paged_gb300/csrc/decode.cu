@@ -40,6 +40,7 @@
 // Reduction kernel: the reduction map's slots of each split output, merged in
 // ascending order with a common maximum (technical review eq 6); used after the
 // prefill kernel and by bsp_run_merge_partials.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <climits>
@@ -149,68 +150,73 @@ struct DecodeParams {
     const float *sink;       // per-qo-head sink logits, or null
 };
 
-// Merge of one reduction-map entry by threads t = 0..nthreads-1 of the CTA that
-// wrote its last partial state: the fold of its slots (technical review §3.2
-// eq 6), final O and LSE written. The partials were written by other CTAs and
-// are read through L2, so the fold is latency-bound: each thread takes one
-// (row, 4 columns) unit and issues the loads of up to 8 slots (their LSEs and
-// float4 columns) before using any, one round trip per 8 slots instead of one
-// per slot. Up to 8 slots this is the fold with one common maximum; longer
-// entries fold 8 slots at a time, rescaling to the running maximum.
-template <int D, typename OutT>
-__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int t, int nthreads) {
+// Fold of one (row r, columns 4 cq .. 4 cq + 3) unit of a reduction-map entry
+// (technical review §3.2 eq 6): its slots' partial states into the final O and
+// LSE. The partials were written by other CTAs and are read through L2, so the
+// fold is latency-bound: the loads of up to 8 slots (their LSEs and float4
+// columns) are issued before any is used, one round trip per 8 slots. Up to 8
+// slots this is the fold with one common maximum; longer entries fold 8 slots
+// at a time, rescaling to the running maximum. Prm: DecodeParams or
+// ReduceParams (workspace offsets, outputs, shapes, sinks).
+template <int D, typename OutT, typename Prm>
+__device__ __forceinline__ void fold_unit(const Prm &p, const bsp_merge_entry &e, int r, int cq) {
     constexpr int kQ = D / 4;     // column quads per row
     constexpr int kBatch = 8;     // slots whose loads are in flight together
     const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
     const float4 *po = reinterpret_cast<const float4 *>(p.ws + p.off_po);
-    const int rows = e.n_pos * p.g;
-    for (int u = t; u < rows * kQ; u += nthreads) {
-        const int r = u / kQ, cq = u - r * kQ;
-        float M = -INFINITY, L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < e.n_slots; s0 += kBatch) {
-            const int ns = min(kBatch, e.n_slots - s0);
-            float l[kBatch];
-            float4 o[kBatch];
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < e.n_slots; s0 += kBatch) {
+        const int ns = min(kBatch, e.n_slots - s0);
+        float l[kBatch];
+        float4 o[kBatch];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const size_t prow = (size_t)(e.slot_begin + s0 + j) * p.tile_rows + r;
-                l[j] = j < ns ? __ldcg(plse + prow) : -INFINITY;
-                o[j] = j < ns ? __ldcg(po + prow * kQ + cq) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            float Mb = M;
+        for (int j = 0; j < kBatch; ++j) {
+            const size_t prow = (size_t)(e.slot_begin + s0 + j) * p.tile_rows + r;
+            l[j] = j < ns ? __ldcg(plse + prow) : -INFINITY;
+            o[j] = j < ns ? __ldcg(po + prow * kQ + cq) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mb = M;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, l[j]);
-            if (Mb == -INFINITY) continue;  // every slot so far empty
-            if (M != Mb) {                   // rescale what was folded to the new maximum
-                const float f = M == -INFINITY ? 0.f : exp2f((M - Mb) * kLog2e);
-                L *= f;
-                acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
-                M = Mb;
-            }
+        for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, l[j]);
+        if (Mb == -INFINITY) continue;  // every slot so far empty
+        if (M != Mb) {                   // rescale what was folded to the new maximum
+            const float f = M == -INFINITY ? 0.f : exp2f((M - Mb) * kLog2e);
+            L *= f;
+            acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+            M = Mb;
+        }
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (j < ns) {
-                    const float wgt = exp2f((l[j] - M) * kLog2e);
-                    L += wgt;
-                    acc.x = fmaf(wgt, o[j].x, acc.x);
-                    acc.y = fmaf(wgt, o[j].y, acc.y);
-                    acc.z = fmaf(wgt, o[j].z, acc.z);
-                    acc.w = fmaf(wgt, o[j].w, acc.w);
-                }
+        for (int j = 0; j < kBatch; ++j) {
+            if (j < ns) {
+                const float wgt = exp2f((l[j] - M) * kLog2e);
+                L += wgt;
+                acc.x = fmaf(wgt, o[j].x, acc.x);
+                acc.y = fmaf(wgt, o[j].y, acc.y);
+                acc.z = fmaf(wgt, o[j].z, acc.z);
+                acc.w = fmaf(wgt, o[j].w, acc.w);
             }
         }
-        float inv = M != -INFINITY ? 1.f / L : 0.f;
-        float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
-        if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
-        const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
-        OutT *dst = static_cast<OutT *>(p.o) + orow * D + cq * 4;
-        dst[0] = from_float<OutT>(acc.x * inv);
-        dst[1] = from_float<OutT>(acc.y * inv);
-        dst[2] = from_float<OutT>(acc.z * inv);
-        dst[3] = from_float<OutT>(acc.w * inv);
-        if (cq == 0 && p.lse) p.lse[orow] = lse_row;
     }
+    float inv = M != -INFINITY ? 1.f / L : 0.f;
+    float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
+    if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
+    const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
+    OutT *dst = static_cast<OutT *>(p.o) + orow * D + cq * 4;
+    dst[0] = from_float<OutT>(acc.x * inv);
+    dst[1] = from_float<OutT>(acc.y * inv);
+    dst[2] = from_float<OutT>(acc.z * inv);
+    dst[3] = from_float<OutT>(acc.w * inv);
+    if (cq == 0 && p.lse) p.lse[orow] = lse_row;
+}
+
+// Merge of one reduction-map entry by threads t = 0..nthreads-1 of the CTA that
+// wrote its last partial state: one (row, 4 columns) unit per thread.
+template <int D, typename OutT>
+__device__ __forceinline__ void merge_entry(const DecodeParams &p, const bsp_merge_entry &e, int t, int nthreads) {
+    constexpr int kQ = D / 4;
+    const int rows = e.n_pos * p.g;
+    for (int u = t; u < rows * kQ; u += nthreads) fold_unit<D, OutT>(p, e, u / kQ, u % kQ);
 }
 
 // Status codes the decode kernel writes to the workspace status word.
@@ -903,46 +909,23 @@ struct ReduceParams {
 
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
-    constexpr int E = D / 32;
     // Launched as a programmatic dependent of the attention kernel: it may be
     // resident before that kernel ends, and waits here until its writes
     // (partial states, the header) are complete and visible.
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    constexpr int kQ = D / 4;
     const DevHeader *hdr = reinterpret_cast<const DevHeader *>(p.ws + p.off_header);
     const bsp_merge_entry *merges = reinterpret_cast<const bsp_merge_entry *>(p.ws + p.off_merges);
-    const float *plse = reinterpret_cast<const float *>(p.ws + p.off_plse);
-    const float *po = reinterpret_cast<const float *>(p.ws + p.off_po);
-    const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    const int total = hdr->num_merges * p.tile_rows;
-    for (int task = gw; task < total; task += nw) {
-        const bsp_merge_entry e = merges[task / p.tile_rows];
-        const int r = task % p.tile_rows;
-        if (r >= e.n_pos * p.g) continue;
-        float M = -INFINITY;
-        for (int s = 0; s < e.n_slots; ++s) M = fmaxf(M, plse[(size_t)(e.slot_begin + s) * p.tile_rows + r]);
-        float acc[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] = 0.f;
-        float L = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < e.n_slots; ++s) {
-                const size_t prow = (size_t)(e.slot_begin + s) * p.tile_rows + r;
-                const float wgt = exp2f((plse[prow] - M) * kLog2e);
-                L += wgt;
-#pragma unroll
-                for (int i = 0; i < E; ++i) acc[i] = fmaf(wgt, po[prow * D + lane * E + i], acc[i]);
-            }
-        }
-        float inv = M != -INFINITY ? 1.f / L : 0.f;
-        float lse_row = M != -INFINITY ? M + logf(L) : -INFINITY;
-        if (p.sink) inv *= fold_sink(lse_row, p.sink[e.kv_head * p.g + r % p.g]);
-        const size_t orow = (size_t)(e.q_tok0 + r / p.g) * p.H_qo + (size_t)e.kv_head * p.g + (r % p.g);
-        OutT *o = static_cast<OutT *>(p.o) + orow * D + lane * E;
-#pragma unroll
-        for (int i = 0; i < E; ++i) o[i] = from_float<OutT>(acc[i] * inv);
-        if (lane == 0 && p.lse) p.lse[orow] = lse_row;
+    // one (row, 4 columns) unit per thread and turn; the grid is sized to the
+    // plan's units when launched, and strides over any plan's
+    const long long units = (long long)hdr->num_merges * p.tile_rows * kQ;
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long rr = u / kQ;
+        const int cq = (int)(u - rr * kQ);
+        const bsp_merge_entry &e = merges[rr / p.tile_rows];
+        const int r = (int)(rr % p.tile_rows);
+        if (r < e.n_pos * p.g) fold_unit<D, OutT>(p, e, r, cq);
     }
 }
 
@@ -987,11 +970,14 @@ int launch_decode_f32(const DecodeParams &p, int grid, cudaStream_t stream) {
 }
 
 template <int D, typename OutT>
-int launch_reduce_t(const ReduceParams &p, cudaStream_t stream) {
+int launch_reduce_t(const ReduceParams &p, int64_t units, cudaStream_t stream) {
     const int sms = num_sms_of_current_device(nullptr);
     if (sms < 0) return fail(BSP_ERR_CUDA, "no current CUDA device");
+    // one unit per thread for this plan (every load in flight at once), at
+    // least two CTAs per SM and at most 64
+    const int64_t want = (units + 255) / 256;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * sms);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(2 * sms, std::min<int64_t>(want, 64 * (int64_t)sms)));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1147,11 +1133,14 @@ int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspac
     p.tile_rows = plan->tile_rows;
     p.sink = P.sink;
     const bool bf = P.dtype == BSP_DTYPE_BF16;
+    const int64_t u = (int64_t)plan->num_merges * plan->tile_rows * (P.head_dim / 4);
     switch (P.head_dim) {
-        case 32: return bf ? launch_reduce_t<32, __nv_bfloat16>(p, stream) : launch_reduce_t<32, float>(p, stream);
-        case 64: return bf ? launch_reduce_t<64, __nv_bfloat16>(p, stream) : launch_reduce_t<64, float>(p, stream);
-        case 128: return bf ? launch_reduce_t<128, __nv_bfloat16>(p, stream) : launch_reduce_t<128, float>(p, stream);
-        case 256: return bf ? launch_reduce_t<256, __nv_bfloat16>(p, stream) : launch_reduce_t<256, float>(p, stream);
+        case 32: return bf ? launch_reduce_t<32, __nv_bfloat16>(p, u, stream) : launch_reduce_t<32, float>(p, u, stream);
+        case 64: return bf ? launch_reduce_t<64, __nv_bfloat16>(p, u, stream) : launch_reduce_t<64, float>(p, u, stream);
+        case 128:
+            return bf ? launch_reduce_t<128, __nv_bfloat16>(p, u, stream) : launch_reduce_t<128, float>(p, u, stream);
+        case 256:
+            return bf ? launch_reduce_t<256, __nv_bfloat16>(p, u, stream) : launch_reduce_t<256, float>(p, u, stream);
         default: return fail(BSP_ERR_UNSUPPORTED, "head_dim must be 32, 64, 128 or 256");
     }
 }
