@@ -60,6 +60,10 @@ constexpr int kRows = 128;        // rows per subtile (M)
 constexpr int kKvTile = 128;      // KV tokens per tile
 constexpr int kD = 128;           // head dim
 constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+// the cp.async gather adds warp 10: warp 0 copies K, warp 10 V (one warp alone
+// cannot keep enough 16-byte copies in flight)
+constexpr int kThreadsGather = 352;
+constexpr int kVWarp = 10;
 constexpr int kHalf = 16384;      // [128 rows][64 bf16], 128-byte swizzle
 constexpr int kTile = 2 * kHalf;  // [128 rows][128 bf16]
 
@@ -159,7 +163,7 @@ __device__ __forceinline__ float ex2(float x) {
 // kVar: the sliding window and logits soft-cap variants are compiled in (the
 // default instantiation has neither, at no cost).
 template <bool kTma, bool kVar>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kTma ? kThreads : kThreadsGather, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     // V ring starts zeroed: rows a tile does not copy then always hold finite values
-    for (int i = threadIdx.x; i < kVStages * kTile / 16; i += kThreads)
+    for (int i = threadIdx.x; i < kVStages * kTile / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(smem + kOffV)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 0 && lane == 0) {
@@ -292,14 +296,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(full) : "memory");
                     };
+                    (void)vst;
+                    (void)vrd;
                     if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
-                    copy_tile(p.k, sb + kOffK + stage * kTile, bar(kKFull0 + stage));
-                    if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
-                    copy_tile(p.v, sb + kOffV + vst * kTile, bar(kVFull0 + vst));
+                    copy_tile(p.k, sb + kOffK + stage * kTile, bar(kKFull0 + stage));  // V: warp kVWarp
                 }
             }
         }
         if constexpr (!kTma) asm volatile("cp.async.wait_all;\n" ::: "memory");  // nothing in flight at exit
+    } else if (!kTma && warp == kVWarp) {
+        // ------------------------------------------------ V gather (cp.async)
+        // The same items and tiles as warp 0, V rows only: lane l looks up keys
+        // l + 32 i one tile ahead, each warp instruction copies two keys' sixteen
+        // 16-byte chunks into their swizzled places.
+        int j = 0;
+        bool ok = true;
+        for (int it = it0; it < it1 && ok; ++it) {
+            const bsp_work_item w = items[it];
+            const int len = w.kv_end - w.kv_start;
+            const int nt = (len + kKvTile - 1) / kKvTile;
+            int pg_next[kKvTile / 32];
+            auto lookup = [&](int (&pg)[kKvTile / 32], int tt) {
+#pragma unroll
+                for (int i = 0; i < kKvTile / 32; ++i) {
+                    const int key = tt * kKvTile + lane + 32 * i;
+                    pg[i] = key < len ? __ldg(p.kv_indices + w.page_base + (w.kv_start + key) / p.page_size) : 0;
+                }
+            };
+            if (nt > 0) lookup(pg_next, 0);
+            for (int t = 0; t < nt; ++t, ++j) {
+                const int tok0 = w.kv_start + t * kKvTile;
+                const int valid = min(kKvTile, len - t * kKvTile);
+                const int vst = j % kVStages, vrd = j / kVStages;
+                uint64_t off[kKvTile / 32];
+#pragma unroll
+                for (int i = 0; i < kKvTile / 32; ++i) {
+                    const int key = lane + 32 * i;
+                    const int tk_ = tok0 + key;
+                    off[i] = key < valid ? (((uint64_t)pg_next[i] * p.page_size + tk_ % p.page_size) * p.H_kv +
+                                            w.kv_head) * (kD * 2)
+                                         : 0;
+                }
+                if (t + 1 < nt) lookup(pg_next, t + 1);
+                if (!(ok = wait_bar_warp(ctx, bar(kVEmpty0 + vst), (vrd & 1) ^ 1))) break;
+                const uint32_t dst = sb + kOffV + vst * kTile;
+                const char *src = p.v;
+                const int c = lane & 15;
+#pragma unroll
+                for (int ii = 0; ii < kKvTile / 2; ++ii) {
+                    const int key = 2 * ii + (lane >> 4);  // key >> 5 == ii >> 4 for the whole warp
+                    const uint64_t o = __shfl_sync(0xffffffffu, off[ii >> 4], key & 31);
+                    if (key < valid)
+                        dev::cp_async_16(dst + (c >> 3) * kHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4),
+                                         src + o + c * 16, 16);
+                }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar(kVFull0 + vst))
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");  // nothing in flight at exit
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         // One thread issues everything: between MMA groups the tensor pipe
@@ -676,7 +731,7 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.num_queues = plan->capacity.num_ctas;
     p.queues_per_cta = (p.num_queues + sms - 1) / sms;
     const int grid = (p.num_queues + p.queues_per_cta - 1) / p.queues_per_cta;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    kern<<<grid, tma ? kThreads : kThreadsGather, kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
     return BSP_OK;
