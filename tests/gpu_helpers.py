@@ -25,13 +25,15 @@ def to_dev(batch, dev="cuda"):
             torch.from_numpy(np.ascontiguousarray(batch.kv_indices, np.int32)).to(dev))
 
 
-def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=None, max_qo=None, sink=None):
+def run_batch(bsp, batch, mode=None, num_ctas=None, dev_tensors=None, max_batch=None, max_qo=None, sink=None,
+              chunks_per_cta=1):
     """Plan + run through the library; returns (O, LSE) on the host and the runner."""
     mode = mode or ("decode" if batch.is_decode else "prefill")
     pa = bsp.PagedAttention(mode, batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
                             batch.causal, TORCH[batch.dtype], max_batch=max_batch or batch.batch,
                             max_qo_tokens=max_qo or int(batch.qo_indptr[-1]), num_ctas=num_ctas,
-                            window_left=batch.window_left, logits_soft_cap=batch.soft_cap)
+                            window_left=batch.window_left, logits_soft_cap=batch.soft_cap,
+                            chunks_per_cta=chunks_per_cta)
     qo = None if mode == "decode" and batch.is_decode else batch.qo_indptr
     pa.plan(batch.kv_indptr, batch.last_page_len, qo_indptr=qo)
     q, k, v, idx = dev_tensors or to_dev(batch)

@@ -110,6 +110,21 @@ def test_tma_gather_equals_cp_async_gather(bsp, ps, D):
     assert torch.equal(out.cuda(), out0) and torch.equal(lse.cuda(), lse0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_many_slot_folds(bsp, dtype):
+    """Plans with many chunks per CTA: outputs split into more than 8 partial
+    states, so the in-kernel fold takes its batches of 8 with rescaling to the
+    running maximum (bf16 and fp32 kernels); against the oracle."""
+    b = workloads.paged_batch(61, np.ones(5, int), [6000, 2500, 17, 900, 4100], 32, 8, 128, 16, dtype,
+                              extra_pages=3)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=11, chunks_per_cta=16)
+    q_, items, merges = pa.plan_arrays()
+    assert int(merges["n_slots"].max()) > 8
+    compare(out, lse, O, L, dtype)
+    assert pa.check_device_error() == 0
+
+
 def test_shared_prefix_full_view_decode(bsp):
     """The shared-prefix batch read without composition (every request over
     prefix + suffix pages), including the 32768-token outlier; sampled rows."""

@@ -143,6 +143,21 @@ def test_ragged_causal_prefill_full_size(bsp):
     assert torch.equal(out, out3) and torch.equal(lse, lse3)
 
 
+def test_many_slot_folds_prefill(bsp):
+    """A causal prefill planned with many chunks per CTA: the reduce kernel folds
+    outputs of 9 to 11 partial states (batches of 8, rescaled to the running
+    maximum); against the oracle."""
+    b = workloads.paged_batch(62, [700, 130, 1], [3000, 130, 1], 32, 8, 128, 16, "bf16", causal=True,
+                              extra_pages=2)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=24, chunks_per_cta=40)
+    _, items, merges = pa.plan_arrays()
+    assert int(merges["n_slots"].max()) > 8
+    n = int(b.qo_indptr[-1])
+    compare(out[:n], lse[:n], O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
 def composable_decode(bsp, sp, num_ctas_prefill=None, num_ctas_decode=None):
     """Prefix view (all queries as one row block over the shared pages, on the
     prefill kernel) and suffix view (decode), merged with merge_state."""
