@@ -750,7 +750,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["ragged_causal_prefill", "fp8_kv_decode", "shared_prefix_decode"], default=None,
+    ap.add_argument("--case", choices=["ragged_causal_prefill", "fp8_kv_decode", "shared_prefix_decode",
+                                       "vector_sparse_prefill"], default=None,
                     help="run one secondary workload alone (steps / warmup as given) and print its line; "
                          "for profiling")
     args = ap.parse_args(argv)
@@ -760,7 +761,7 @@ def main(argv=None):
         import block_sparse_paged_gb300 as bsp
         dev = torch.device("cuda", 0)
         fn = {"ragged_causal_prefill": ragged_prefill, "fp8_kv_decode": fp8_decode,
-              "shared_prefix_decode": shared_prefix}[args.case]
+              "shared_prefix_decode": shared_prefix, "vector_sparse_prefill": vector_sparse_prefill}[args.case]
         print(json.dumps({args.case: fn(bsp, dev, args.steps, args.warmup, peaks()[0])}), flush=True)
         return
     rank, world, local = dist_setup()
