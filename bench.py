@@ -145,13 +145,14 @@ class ClockSampler:
             os.unlink(self.path)
         except OSError:
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             r = [x.strip() for x in r]
             try:
                 sm.append(float(r[1]))
                 mx.append(float(r[2]))
+                pw.append(float(r[3]))
             except (ValueError, IndexError):
                 continue
             for n, v in zip(names, r[5:9]):
@@ -160,7 +161,21 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None}
+
+
+def clocks_while(run, seconds: float, gpu_index: int):
+    """SM clocks (ClockSampler) while run() is called back to back for about
+    `seconds`: the clock a kernel holds under its own sustained load."""
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_index).start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            run()
+        torch.cuda.synchronize()
+    return sampler.stop()
 
 
 def kernel_digest(*names) -> str:
@@ -409,37 +424,118 @@ def run_e2e(bsp, batch, pa, K, W, dev, nbytes, world):
             "note": "KV pool, Q and page table copied from pinned host memory every step"}
 
 
-def cpu_baseline(batch, seconds: float):
-    """The oracle, as it stands, on all host cores over the full workload,
-    repeated for about `seconds`."""
+def oracle_timed(batch, tok, head, seconds: float, threads: int = 0):
+    """(repetitions, seconds) of the oracle, as it stands, over the selected
+    (token, head) rows, repeated for about `seconds` (at least once)."""
     import oracle
     k32 = batch.k_pages.float().numpy()
     v32 = batch.v_pages.float().numpy()
-    n_tok = int(batch.qo_indptr[-1])
-    tok = np.repeat(np.arange(n_tok, dtype=np.int64), batch.num_qo_heads)
-    head = np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), n_tok)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.attention_rows_of(batch, tok, head, k_f32=k32, v_f32=v32)
+        oracle.attention_rows_of(batch, tok, head, num_threads=threads, k_f32=k32, v_f32=v32)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 1000:
-            break
+            return reps, el
+
+
+def all_rows(batch, n_req=None):
+    """(token, head) of every output row of the first n_req requests (all by default)."""
+    n_tok = int(batch.qo_indptr[batch.batch if n_req is None else n_req])
+    return (np.repeat(np.arange(n_tok, dtype=np.int64), batch.num_qo_heads),
+            np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), n_tok))
+
+
+def strided_rows(batch, stride: int, seed: int):
+    """(token, head): every stride-th query position of each request and head,
+    with a seeded phase per (request, head): a 1/stride sample of every request
+    and head."""
+    rng = np.random.default_rng(seed)
+    toks, heads = [], []
+    for b in range(batch.batch):
+        q0, q1 = int(batch.qo_indptr[b]), int(batch.qo_indptr[b + 1])
+        for h in range(batch.num_qo_heads):
+            sel = np.arange(q0 + int(rng.integers(stride)), q1, stride, dtype=np.int64)
+            toks.append(sel)
+            heads.append(np.full(sel.size, h, np.int32))
+    return np.concatenate(toks), np.concatenate(heads)
+
+
+def row_flops(batch, tok) -> float:
+    """4 * D per visible (query, key) pair of the selected rows (one head each)."""
+    b = np.searchsorted(batch.qo_indptr, tok, side="right") - 1
+    qo, kv = batch.qo_lens[b], batch.kv_lens[b]
+    if batch.causal:
+        vis = np.clip(tok - batch.qo_indptr[b] + kv - qo + 1, 0, kv)
+    else:
+        vis = kv
+    return 4.0 * batch.head_dim * float(np.sum(vis))
+
+
+def cpu_baseline(batch, seconds: float):
+    """The oracle, as it stands, on all host cores over the full workload,
+    repeated for about `seconds`; then on one core over the first 4 requests."""
+    import oracle
+    tok, head = all_rows(batch)
+    reps, el = oracle_timed(batch, tok, head, seconds)
     gbs = decode_bytes(batch) * reps / el / 1e9
+    sub = workloads_sub(batch, 4)
+    t1, h1 = all_rows(batch, 4)
+    r1, e1 = oracle_timed(batch, t1, h1, seconds / 4, threads=1)
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.num_threads_available(), "kind": "oracle",
-            "sample": f"full workload (64 requests x 32 heads), {reps} repetitions in {el:.1f} s, fp64"}
+            "sample": f"full workload (64 requests x 32 heads), {reps} repetitions in {el:.1f} s, fp64",
+            "one_core": {"value": round(decode_bytes(sub) * r1 / e1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                         "sample": f"first 4 requests x 32 heads, {r1} repetitions in {e1:.1f} s, fp64"}}
+
+
+def workloads_sub(batch, n_req):
+    """The first n_req requests of a batch (same pools)."""
+    import workloads
+    return workloads.scaled(batch, qo_indptr=batch.qo_indptr[:n_req + 1], kv_indptr=batch.kv_indptr[:n_req + 1],
+                            last_page_len=batch.last_page_len[:n_req])
+
+
+def cpu_baseline_prefill(batch, stride: int, seed: int, seconds: float):
+    """The oracle on all host cores over a seeded 1/stride sample of the rows
+    (every request and head), repeated for about `seconds`: GFLOP/s over the
+    sampled rows' visible pairs."""
+    import oracle
+    tok, head = strided_rows(batch, stride, seed)
+    reps, el = oracle_timed(batch, tok, head, seconds)
+    fl = row_flops(batch, tok)
+    return {"value": round(fl * reps / el / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.num_threads_available(),
+            "kind": "oracle",
+            "sample": f"every {stride}th query position of every request and head (seeded phase, seed {seed}): "
+                      f"{tok.size} rows, {fl:.3e} FLOP, {reps} repetitions in {el:.1f} s, fp64"}
 
 
 def secondary(bsp, dev, args, pk):
-    import workloads
     res = {}
     steps = max(5, min(args.steps, 50))
     warm = max(3, args.warmup)
-    # page size 1, permuted vs contiguous
+    cpu = 0.0 if args.no_cpu_baseline else args.cpu_seconds / 2
+    res["vector_sparse_decode"] = vector_sparse_decode(bsp, dev, steps, warm, pk, args.num_ctas)
+    torch.cuda.empty_cache()
+    res["ragged_causal_prefill"] = ragged_prefill(bsp, dev, steps, warm, pk, cpu)
+    torch.cuda.empty_cache()
+    res["vector_sparse_prefill"] = vector_sparse_prefill(bsp, dev, max(3, steps // 10), warm, pk, cpu)
+    torch.cuda.empty_cache()
+    res["bsr_prefill"] = bsr_prefill(bsp, dev, steps, warm, pk, cpu)
+    torch.cuda.empty_cache()
+    res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
+    res["fp8_kv_decode"] = fp8_decode(bsp, dev, steps, warm, pk)
+    res["tiny_decode_f32"] = tiny_decode_f32(bsp, dev, steps, warm, pk)
+    return res
+
+
+def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0.0):
+    """Page size 1 (every token slot permuted) vs the same KV contiguous: GB/s
+    of each and their ratio."""
+    import workloads
     perm, cont = workloads.vector_sparse_decode_bf16()
     r = {}
     for tag, b in (("permuted", perm), ("contiguous", cont)):
-        C = args.num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
+        C = num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
         pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, 1, False, torch.bfloat16,
                                 max_batch=b.batch, num_ctas=C, device=dev)
         pa.plan(b.kv_indptr, b.last_page_len)
@@ -456,11 +552,18 @@ def secondary(bsp, dev, args, pk):
     r["permuted_over_contiguous"] = round(r["permuted"]["GB/s"] / r["contiguous"]["GB/s"], 4)
     r["workload"] = ("32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16; "
                      "one launch per run, 10 per graph replay")
-    res["vector_sparse_decode"] = r
-    del perm, cont
-    res["ragged_causal_prefill"] = ragged_prefill(bsp, dev, steps, warm, pk)
-    torch.cuda.empty_cache()
-    res["vector_sparse_prefill"] = vector_sparse_prefill(bsp, dev, max(3, steps // 10), warm, pk)
+    r["roofline"] = {"bound": "hbm", "kernel": "decode_bf16_kernel<128, cp.async gather>",
+                     "achieved": r["permuted"]["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": r["permuted"]["frac_of_hbm"], "peak_source": "measured (STREAM-style copy)",
+                     "traffic": profile_traffic("decode_vector_sparse", kernel_digest(*DECODE_SOURCES)),
+                     "algorithmic_bytes_per_launch": decode_bytes(perm)}
+    return r
+
+
+def bsr_prefill(bsp, dev, steps, warm, pk, cpu_seconds=0.0):
+    """General BSR prefill (row blocks of 64 queries, 16-token column blocks,
+    25% density), graph-timed."""
+    import workloads
     b = workloads.bsr_prefill_bf16()
     pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
                             torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
@@ -473,19 +576,40 @@ def secondary(bsp, dev, args, pk):
     ms = graph_time(lambda: pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, stream=st), st, steps, warm)
     fl = prefill_flops(b)
     tf = fl / (ms * 1e-3) / 1e12
-    res["bsr_prefill"] = {"TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-                          "ms": round(ms, 4), "flops": fl,
-                          "workload": "general BSR: 32 row blocks of 64 queries, 512 column blocks of 16 tokens, "
-                                      "25% block density, 32/8 heads, D 128, bf16, non-causal; "
-                                      "10 runs per graph replay"}
-    del b, pa, q, k, v, out, lse
-    torch.cuda.empty_cache()
-    res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
-    res["fp8_kv_decode"] = fp8_decode(bsp, dev, steps, warm, pk)
-    return res
+    r = {"TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+         "ms": round(ms, 4), "flops": fl,
+         "workload": "general BSR: 32 row blocks of 64 queries, 512 column blocks of 16 tokens, "
+                     "25% block density, 32/8 heads, D 128, bf16, non-causal; 10 runs per graph replay",
+         "roofline": {"bound": "tensor", "kernel": "prefill_kernel<TMA>", "achieved": round(tf, 1),
+                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
+                      "peak_source": "measured (cuBLAS bf16 burst)",
+                      "traffic": profile_traffic("prefill_bsr", kernel_digest(*PREFILL_SOURCES)),
+                      "algorithmic_flops_per_launch": fl}}
+    del pa, q, k, v, out, lse
+    if cpu_seconds > 0:
+        r["cpu_baseline"] = cpu_baseline_prefill(b, 8, 7, cpu_seconds)
+    return r
 
 
-def ragged_prefill(bsp, dev, steps, warm, pk):
+def tiny_decode_f32(bsp, dev, steps, warm, pk):
+    """The tiny fp32 paged decode (3 requests, KV 10 / 3 / 7, page 4, 4/2 heads,
+    D 64): latency of one run (graph-timed), correctness-sized."""
+    import workloads
+    b = workloads.tiny_decode_f32()
+    pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, False,
+                            torch.float32, max_batch=b.batch, device=dev)
+    pa.plan(b.kv_indptr, b.last_page_len)
+    q, k, v, idx = to_dev(b, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    ms = graph_time(lambda: pa.run(q, k, v, idx, b.sm_scale, out=out, lse=lse, stream=st), st, steps, warm)
+    return {"us": round(ms * 1e3, 2), "bytes": decode_bytes(b), "kernel": "decode_f32_kernel",
+            "workload": "3 requests, KV 10 / 3 / 7, page 4 (16-page permuted pool), 4/2 heads, D 64, fp32; "
+                        "10 runs per graph replay"}
+
+
+def ragged_prefill(bsp, dev, steps, warm, pk, cpu_seconds=0.0):
     """The ragged causal prefill workload, kernel-only timing with a roofline.
     Planned for two LPT queues per CTA (each CTA runs two consecutive queues):
     swept on GB300 (graph-timed, alpha 2), 152 / 304 / 456 queues 279.4 /
@@ -496,15 +620,20 @@ def ragged_prefill(bsp, dev, steps, warm, pk):
     pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
                             torch.bfloat16, max_batch=b.batch, max_qo_tokens=int(b.qo_indptr[-1]), num_ctas=C,
                             device=dev)
-    attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
+    dev_t = to_dev(b, dev)
+    attn, merge, out, lse = time_kernel_only(pa, b, dev_t, steps, warm, qo=b.qo_indptr)
     fl = prefill_flops(b)
     tf = fl / ((attn + merge) * 1e-3) / 1e12
     ka = fl / (attn * 1e-3) / 1e12
-    return {
+    clk = clocks_while(lambda: pa.run_stages(*dev_t, b.sm_scale, out, lse), 1.5, dev.index or 0)
+    del pa
+    cpu = cpu_baseline_prefill(b, 8, 4, cpu_seconds) if cpu_seconds > 0 else None
+    return {"cpu_baseline": cpu,
         "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "flops": fl,
         "attn_ms": round(attn, 4), "merge_ms": round(merge, 4),
         "workload": "16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, D 128, bf16, causal; "
                     "plan of 2 queues per CTA", "plan_queues": C,
+        "clocks_sustained": clk,
         "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(ka, 1),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ka / pk["bf16_tflops"], 4),
                      "peak_source": "measured (cuBLAS bf16 burst; the kernel is timed alone)",
@@ -573,9 +702,13 @@ def fp8_decode(bsp, dev, steps, warm, pk):
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
-def vector_sparse_prefill(bsp, dev, steps, warm, pk):
-    """One 32768-token causal prefill with page size 1 (cp.async gather), once on
-    permuted slots and once contiguous: TFLOP/s of each and their ratio."""
+def vector_sparse_prefill(bsp, dev, steps, warm, pk, cpu_seconds=0.0):
+    """One 32768-token causal prefill with page size 1, once on permuted slots and
+    once contiguous, each planned with a gather region for its page table (the
+    pages are copied into the workspace in table order, then read by TMA; the
+    copy is inside the timed run), and once permuted without a region (16-byte
+    cp.async gather): TFLOP/s of each, their ratios, and the same KV as
+    128-token pages (TMA page gather, no copy)."""
     import workloads
     import dataclasses
     perm, cont = workloads.vector_sparse_prefill_bf16()
@@ -588,9 +721,11 @@ def vector_sparse_prefill(bsp, dev, steps, warm, pk):
                                 v_pages=cont.v_pages.reshape(n // 128, 128, cont.num_kv_heads, cont.head_dim))
     fl = prefill_flops(perm)
     r = {}
-    for tag, b in (("permuted", perm), ("contiguous", cont), ("contiguous_pages128", dense)):
+    for tag, b, region in (("permuted", perm, n), ("contiguous", cont, n), ("permuted_cp_async", perm, 0),
+                           ("contiguous_pages128", dense, 0)):
         pa = bsp.PagedAttention("prefill", b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, True,
-                                torch.bfloat16, max_batch=1, max_qo_tokens=int(b.qo_indptr[-1]), device=dev)
+                                torch.bfloat16, max_batch=1, max_qo_tokens=int(b.qo_indptr[-1]), device=dev,
+                                max_gather_pages=region)
         attn, merge, _, _ = time_kernel_only(pa, b, to_dev(b, dev), steps, warm, qo=b.qo_indptr)
         tf = fl / ((attn + merge) * 1e-3) / 1e12
         r[tag] = {"TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
@@ -600,9 +735,12 @@ def vector_sparse_prefill(bsp, dev, steps, warm, pk):
     r["permuted_over_contiguous"] = round(r["permuted"]["TFLOP/s"] / r["contiguous"]["TFLOP/s"], 4)
     r["page1_over_pages128"] = round(r["permuted"]["TFLOP/s"] / r["contiguous_pages128"]["TFLOP/s"], 4)
     r["flops"] = fl
-    r["workload"] = ("1 request, qo = kv = 32768, causal, page size 1 (slots permuted / contiguous; cp.async gather) "
-                     "and the same KV as 128-token pages (TMA gather), 32/8 heads, D 128, bf16")
+    r["workload"] = ("1 request, qo = kv = 32768, causal, page size 1 (slots permuted / contiguous; page copy into "
+                     "the workspace + TMA, or cp.async gather) and the same KV as 128-token pages (TMA page gather), "
+                     "32/8 heads, D 128, bf16")
     r["pages_context"] = "FA3 template on H100: 532 (page 1) vs 627 (contiguous) TFLOP/s"
+    if cpu_seconds > 0:
+        r["cpu_baseline"] = cpu_baseline_prefill(perm, 128, 6, cpu_seconds)
     return r
 
 
@@ -740,6 +878,12 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# secondary workloads that `--case` runs alone (profiling)
+CASES = {"ragged_causal_prefill": ragged_prefill, "fp8_kv_decode": fp8_decode, "shared_prefix_decode": shared_prefix,
+         "vector_sparse_prefill": vector_sparse_prefill, "vector_sparse_decode": vector_sparse_decode,
+         "bsr_prefill": bsr_prefill, "tiny_decode_f32": tiny_decode_f32}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -750,8 +894,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["ragged_causal_prefill", "fp8_kv_decode", "shared_prefix_decode",
-                                       "vector_sparse_prefill"], default=None,
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one secondary workload alone (steps / warmup as given) and print its line; "
                          "for profiling")
     args = ap.parse_args(argv)
@@ -760,9 +903,7 @@ def main(argv=None):
         build.build()
         import block_sparse_paged_gb300 as bsp
         dev = torch.device("cuda", 0)
-        fn = {"ragged_causal_prefill": ragged_prefill, "fp8_kv_decode": fp8_decode,
-              "shared_prefix_decode": shared_prefix, "vector_sparse_prefill": vector_sparse_prefill}[args.case]
-        print(json.dumps({args.case: fn(bsp, dev, args.steps, args.warmup, peaks()[0])}), flush=True)
+        print(json.dumps({args.case: CASES[args.case](bsp, dev, args.steps, args.warmup, peaks()[0])}), flush=True)
         return
     rank, world, local = dist_setup()
     if args.impl == "reference":

@@ -44,7 +44,7 @@ class Problem(ctypes.Structure):
 
 class Capacity(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("max_qo_tokens", ctypes.c_int64),
-                ("chunks_per_cta", ctypes.c_int32)]
+                ("chunks_per_cta", ctypes.c_int32), ("max_gather_pages", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -57,7 +57,9 @@ class PlanInfo(ctypes.Structure):
                 ("off_items", ctypes.c_uint64), ("off_merges", ctypes.c_uint64), ("off_status", ctypes.c_uint64),
                 ("off_partial_lse", ctypes.c_uint64), ("off_partial_o", ctypes.c_uint64),
                 ("metadata_bytes", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64),
-                ("valid", ctypes.c_int32), ("num_qo_tokens", ctypes.c_int32)]
+                ("valid", ctypes.c_int32), ("num_qo_tokens", ctypes.c_int32),
+                ("num_table_pages", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("off_gather", ctypes.c_uint64), ("gather_pool_bytes", ctypes.c_uint64)]
 
 
 # numpy views of the plan's staging image (bsp_work_item, bsp_merge_entry)

@@ -157,6 +157,12 @@ extern "C" int bsp_check_device_error(const bsp_plan_info *plan, void *workspace
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e == cudaSuccess && word != 0) {
         e = cudaMemsetAsync(status, 0, sizeof(word), stream);
+        // CTAs that gave up may have left partial counts in the reduction map's
+        // arrival words; a later run of this plan would then fold too early
+        if (e == cudaSuccess && plan->num_merges > 0)
+            e = cudaMemset2DAsync(static_cast<uint8_t *>(workspace) + plan->off_merges +
+                                      offsetof(bsp_merge_entry, arrived),
+                                  sizeof(bsp_merge_entry), 0, sizeof(int32_t), (size_t)plan->num_merges, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     }
     if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));

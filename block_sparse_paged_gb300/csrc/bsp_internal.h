@@ -39,7 +39,9 @@ struct Layout {
     int64_t cap_items = 0, cap_merges = 0, cap_partials = 0;
     uint64_t off_header = 0, off_queue_indptr = 0, off_items = 0, off_merges = 0;
     uint64_t metadata_end = 0;  // staging buffer size
-    uint64_t off_status = 0, off_partial_lse = 0, off_partial_o = 0, total = 0;
+    uint64_t off_status = 0, off_partial_lse = 0, off_partial_o = 0;
+    uint64_t off_gather = 0, gather_pool_bytes = 0;  // K copy region, then V (prefill, optional)
+    uint64_t total = 0;
 };
 
 // Validates the static problem; returns false and sets the error message.
@@ -75,6 +77,11 @@ int launch_decode_fp8(const bsp_plan_info *plan, const void *q, const void *k_pa
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages,
                    const void *v_pages, const int32_t *kv_indices, int64_t num_pages,
                    float sm_scale, void *o, float *lse, void *workspace, cudaStream_t stream);
+// Copy the page table's first n_pages pages of K and V, in table order, into
+// the plan's gather region (prefill with a region); ids outside [0, num_pages)
+// give zero pages and set the workspace status word.
+int launch_gather_pages(const bsp_plan_info *plan, const void *k_pages, const void *v_pages,
+                        const int32_t *kv_indices, int64_t num_pages, void *workspace, cudaStream_t stream);
 int launch_wait_probe(long long limit_cycles, int *status, cudaStream_t stream);
 int launch_reduce(const bsp_plan_info *plan, void *o, float *lse, void *workspace,
                   cudaStream_t stream);

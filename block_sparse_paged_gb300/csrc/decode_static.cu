@@ -1,14 +1,13 @@
 // Decode run for callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc on the path where they run attention:
-// a host framework that has already handed all device memory to its own pool
-// (the KV cache manager of a serving engine usually reserves nearly all of
-// HBM up front) and forbids allocation while serving a request, or code that
-// runs while a stream is being captured in global capture mode, where
-// cudaMalloc is not allowed. Such a caller can still plan on the host and
-// pass its inputs and outputs; this entry point then keeps the run's scratch
-// (the plan metadata and the partial states of split outputs) in a fixed
-// array in device memory that the library itself declares.
+// a serving engine whose KV-cache manager reserved nearly all of HBM up front
+// for its own pool and forbids further allocation while it serves requests,
+// or a plugin that its host hands only the input and output tensors, with no
+// allocator to draw scratch from. Such a caller can still plan on the host
+// and pass its inputs and outputs; this entry point then keeps the run's
+// scratch (the plan metadata and the partial states of split outputs) in a
+// fixed array in device memory that the library itself declares.
 //
 // The array is a file-scope __device__ variable of BSP_STATIC_WORKSPACE_BYTES:
 // every GPU that loads the library holds it until the process exits. Its
@@ -64,6 +63,13 @@ extern "C" int bsp_decode_run_static(const bsp_plan_info *plan, const void *host
     Layout l;
     if (!compute_layout(&plan->problem, &plan->capacity, &l)) return last_code();
     if (l.total != plan->workspace_bytes || l.off_partial_o != plan->off_partial_o)
+        return fail(BSP_ERR_INVALID_ARG, "plan info is inconsistent with its problem and capacity");
+    // The plan's counts and offsets decide where the copies below write into
+    // the shared array: accept only those of the layout its bounds define.
+    if (plan->off_header != l.off_header || plan->off_queue_indptr != l.off_queue_indptr || plan->off_items != l.off_items ||
+        plan->off_merges != l.off_merges || plan->off_status != l.off_status ||
+        plan->off_partial_lse != l.off_partial_lse || plan->num_items < 0 || plan->num_items > l.cap_items ||
+        plan->num_merges < 0 || plan->num_merges > l.cap_merges)
         return fail(BSP_ERR_INVALID_ARG, "plan info is inconsistent with its problem and capacity");
     if (plan->workspace_bytes > BSP_STATIC_WORKSPACE_BYTES)
         return fail(BSP_ERR_CAPACITY, "the plan's workspace (bsp_workspace_size) exceeds the static workspace "

@@ -48,6 +48,10 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
         return fail(BSP_ERR_INVALID_ARG, "capacity needs max_batch >= 0, num_ctas >= 1, max_qo_tokens >= 0"), false;
     if (c->chunks_per_cta < 0 || c->chunks_per_cta > 64)
         return fail(BSP_ERR_INVALID_ARG, "capacity.chunks_per_cta must be in [0, 64]"), false;
+    if (c->max_gather_pages < 0 || (c->max_gather_pages > 0 && p->mode != BSP_MODE_PREFILL))
+        return fail(BSP_ERR_INVALID_ARG, "capacity.max_gather_pages must be >= 0, and 0 in decode mode"), false;
+    if ((int64_t)c->max_gather_pages * p->page_size > INT32_MAX)
+        return fail(BSP_ERR_CAPACITY, "capacity.max_gather_pages x page_size beyond int32 rows"), false;
     const int64_t sC = (int64_t)chunks_per_cta(c) * c->num_ctas;
     const int g = p->num_qo_heads / p->num_kv_heads;
     Layout l;
@@ -82,6 +86,13 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
     off = align_up(off + sizeof(float) * (uint64_t)l.cap_partials * l.tile_rows, kAlign);
     l.off_partial_o = off;
     off = align_up(off + sizeof(float) * (uint64_t)l.cap_partials * l.tile_rows * p->head_dim, kAlign);
+    if (c->max_gather_pages > 0) {
+        const uint64_t esz = p->dtype == BSP_DTYPE_BF16 ? 2 : 4;
+        l.gather_pool_bytes = align_up((uint64_t)c->max_gather_pages * p->page_size * p->num_kv_heads *
+                                           p->head_dim * esz, kAlign);
+        l.off_gather = off;
+        off += 2 * l.gather_pool_bytes;
+    }
     l.total = off;
     *L = l;
     return true;
@@ -314,6 +325,9 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
     o.metadata_bytes = lay.metadata_end;
     o.workspace_bytes = lay.total;
     o.num_qo_tokens = qo[batch];
+    o.num_table_pages = kv_indptr_h[batch];
+    o.off_gather = lay.off_gather;
+    o.gather_pool_bytes = lay.gather_pool_bytes;
     o.valid = ws ? 1 : 2;  // 2: host-only plan, not runnable
     return BSP_OK;
 }

@@ -42,6 +42,7 @@
 // without further work.
 #include <cuda.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -103,6 +104,8 @@ struct PrefillParams {
     float scale_log2;
     int H_qo, H_kv, g, page_size, box_rows, causal, tile_rows;
     int queues_per_cta, num_queues;  // CTA b runs plan queues [b * qpc, min((b + 1) * qpc, C))
+    int contig;              // K / V tensor maps cover the gather region: request b's token t is row
+                             // page_base * page_size + t (boxes of 128 rows, no page lookup)
     int window_left;         // > 0: key j is masked for a row at position i if j < i + kv_len - qo_len - window_left
     int soft_cap_on;         // scores become tanh(s * cap_in); scale_log2 is then c * log2(e)
     float cap_in;            // sm_scale / c
@@ -247,9 +250,15 @@ __global__ void __launch_bounds__(kTma ? kThreads : kThreadsGather, 1)
                 const int vst = j % kVStages, vrd = j / kVStages;
                 if constexpr (kTma) {
                     const int nseg = (valid + p.box_rows - 1) / p.box_rows;
-                    int page = 0;
-                    if (lane < nseg) page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
-                    const int row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
+                    int row0;
+                    if (p.contig) {
+                        row0 = w.page_base * p.page_size + tok0 + lane * p.box_rows;
+                    } else {
+                        int page = 0;
+                        if (lane < nseg)
+                            page = __ldg(p.kv_indices + w.page_base + (tok0 + lane * p.box_rows) / p.page_size);
+                        row0 = page * p.page_size + (tok0 + lane * p.box_rows) % p.page_size;
+                    }
                     const uint32_t seg = (uint32_t)lane * p.box_rows * 128;
                     const uint32_t bytes = (uint32_t)nseg * p.box_rows * 128 * 2;
                     if (!(ok = wait_bar_warp(ctx, bar(kKEmpty0 + stage), (round & 1) ^ 1))) break;
@@ -660,7 +669,73 @@ __global__ void __launch_bounds__(kTma ? kThreads : kThreadsGather, 1)
     }
 }
 
+// Copy of the page table's pages into the gather region, in table order: one
+// warp per page (grid-stride), its id read once, then the page's K and V as
+// 16-byte vectors with 8 loads per lane in flight. HBM-bound: one read and one
+// write of every table page.
+constexpr int kStatusGatherIndex = 0x301;
+
+__global__ void __launch_bounds__(256) gather_pages_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                           uint4 *__restrict__ gk, uint4 *__restrict__ gv,
+                                                           const int32_t *__restrict__ idx, int n_pages,
+                                                           long long num_pages, int page_vecs, int *status) {
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long pg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; pg < n_pages; pg += nwarps) {
+        const int id = __ldg(idx + pg);
+        const bool ok = id >= 0 && id < num_pages;
+        if (!ok && lane == 0) atomicCAS(status, 0, kStatusGatherIndex);
+        const uint4 *sk = k + (ok ? (long long)id * page_vecs : 0), *sv = v + (ok ? (long long)id * page_vecs : 0);
+        uint4 *dk = gk + pg * page_vecs, *dv = gv + pg * page_vecs;
+        for (int base = 0; base < page_vecs; base += 4 * 32) {
+            uint4 a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = base + i * 32 + lane;
+                a[i] = b[i] = make_uint4(0, 0, 0, 0);
+                if (ok && e < page_vecs) {
+                    a[i] = __ldg(sk + e);
+                    b[i] = __ldg(sv + e);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = base + i * 32 + lane;
+                if (e < page_vecs) {
+                    dk[e] = a[i];
+                    dv[e] = b[i];
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+int launch_gather_pages(const bsp_plan_info *plan, const void *k_pages, const void *v_pages,
+                        const int32_t *kv_indices, int64_t num_pages, void *workspace, cudaStream_t stream) {
+    const bsp_problem &P = plan->problem;
+    const int n = plan->num_table_pages;
+    if (n <= 0) return BSP_OK;
+    if (!kv_indices) return fail(BSP_ERR_INVALID_ARG, "kv_indices is NULL but the page table has pages");
+    if (!plan->off_gather || n > plan->capacity.max_gather_pages)
+        return fail(BSP_ERR_CAPACITY, "page table exceeds capacity.max_gather_pages");
+    const int64_t page_bytes = (int64_t)P.page_size * P.num_kv_heads * P.head_dim * (P.dtype == BSP_DTYPE_BF16 ? 2 : 4);
+    if (page_bytes % 16 != 0 || reinterpret_cast<uintptr_t>(k_pages) % 16 || reinterpret_cast<uintptr_t>(v_pages) % 16)
+        return fail(BSP_ERR_INVALID_ARG, "page pools must be 16-byte aligned for the gather");
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return fail(BSP_ERR_CUDA, "no current CUDA device");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t blocks = std::min<int64_t>((n + 7) / 8, (int64_t)sms * 16);
+    gather_pages_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(k_pages), static_cast<const uint4 *>(v_pages),
+        reinterpret_cast<uint4 *>(ws + plan->off_gather), reinterpret_cast<uint4 *>(ws + plan->off_gather + plan->gather_pool_bytes),
+        kv_indices, n, (long long)num_pages, (int)(page_bytes / 16), reinterpret_cast<int *>(ws + plan->off_status));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BSP_ERR_CUDA, std::string("gather launch: ") + cudaGetErrorString(e));
+    return BSP_OK;
+}
 
 int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages, const void *v_pages,
                    const int32_t *kv_indices, int64_t num_pages, float sm_scale, void *o, float *lse,
@@ -672,18 +747,31 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     if (plan->tile_rows != kSub * kRows || kRows % g != 0)
         return fail(BSP_ERR_UNSUPPORTED, "prefill needs 256-row tiles and 128 % g == 0");
     // Pages of 8 or more tokens (powers of two) are gathered by TMA, one tensor
-    // copy per page box; other page sizes by 16-byte cp.async.
+    // copy per page box. Other page sizes: when the workspace has a gather
+    // region that holds the page table, the pages are first copied into it in
+    // table order, and every request's keys are then one contiguous run of
+    // rows read by 128-row TMA boxes; otherwise 16-byte cp.async copies.
     const int ps = P.page_size;
-    const bool tma = ps >= 8 && (ps & (ps - 1)) == 0 && num_pages * (int64_t)ps <= INT32_MAX;
+    const bool direct = ps >= 8 && (ps & (ps - 1)) == 0 && num_pages * (int64_t)ps <= INT32_MAX;
+    const bool gather = !direct && plan->off_gather != 0 && plan->num_table_pages <= plan->capacity.max_gather_pages;
+    const bool tma = direct || gather;
 
     CUtensorMap tq, tk, tv;
     std::memset(&tk, 0, sizeof(tk));
     std::memset(&tv, 0, sizeof(tv));
-    const int box_rows = tma ? (ps < kKvTile ? ps : kKvTile) : 1;
+    const int box_rows = gather ? kKvTile : tma ? (ps < kKvTile ? ps : kKvTile) : 1;
     int rc = make_tmap_bf16(&tq, q, kD, P.num_qo_heads, (uint64_t)(plan->num_qo_tokens > 0 ? plan->num_qo_tokens : 1), g,
                       kRows / g);
-    if (tma && rc == BSP_OK) rc = make_tmap_bf16(&tk, k_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
-    if (tma && rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
+    if (gather) {
+        const uint8_t *region = static_cast<const uint8_t *>(workspace) + plan->off_gather;
+        const uint64_t rows = (uint64_t)plan->capacity.max_gather_pages * ps;
+        if (rc == BSP_OK) rc = make_tmap_bf16(&tk, region, kD, P.num_kv_heads, rows, 1, box_rows);
+        if (rc == BSP_OK) rc = make_tmap_bf16(&tv, region + plan->gather_pool_bytes, kD, P.num_kv_heads, rows, 1, box_rows);
+        if (rc == BSP_OK) rc = launch_gather_pages(plan, k_pages, v_pages, kv_indices, num_pages, workspace, stream);
+    } else if (tma) {
+        if (rc == BSP_OK) rc = make_tmap_bf16(&tk, k_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
+        if (rc == BSP_OK) rc = make_tmap_bf16(&tv, v_pages, kD, P.num_kv_heads, (uint64_t)num_pages * ps, 1, box_rows);
+    }
     if (rc != BSP_OK) return rc;
 
     PrefillParams p;
@@ -709,6 +797,7 @@ int launch_prefill(const bsp_plan_info *plan, const void *q, const void *k_pages
     p.g = g;
     p.page_size = P.page_size;
     p.box_rows = box_rows;
+    p.contig = gather ? 1 : 0;
     p.causal = P.causal;
     p.tile_rows = plan->tile_rows;
 

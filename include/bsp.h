@@ -126,6 +126,21 @@ typedef struct bsp_capacity {
                                (s = 1 is the pages' L = ceil(W / C)). Bounds the
                                work items by tiles + s C and the partial slots
                                by 2 s C; at most 64                            */
+    int32_t max_gather_pages; /* prefill only (0 in decode): pages of the K / V
+                               copy region the workspace reserves, each pool
+                               max_gather_pages x page_size x H_kv x D
+                               elements. 0: no region. With a region, a prefill
+                               run whose pages the TMA page gather cannot take
+                               (pages under 8 tokens or not a power of two)
+                               and whose page table has at most this many
+                               pages (kv_indptr[batch]) first copies the
+                               table's pages, in table order, into the region
+                               and then reads every request's keys as one
+                               contiguous run of rows by TMA. That costs one
+                               read and one write of the table's K and V, and
+                               pays when each KV token is read by several
+                               query tiles (long prefills); larger tables run
+                               the cp.async gather as without a region      */
 } bsp_capacity;
 
 /* One work item of the plan (64 bytes, device and staging image). */
@@ -181,6 +196,11 @@ typedef struct bsp_plan_info {
     uint64_t workspace_bytes;
     int32_t valid;           /* 1: planned and copied; 2: host-only plan      */
     int32_t num_qo_tokens;   /* qo_indptr[batch]: rows of q and o             */
+    int32_t num_table_pages; /* kv_indptr[batch]: entries of kv_indices used  */
+    int32_t reserved0;
+    uint64_t off_gather;     /* K copy region (the V region follows it at
+                                off_gather + gather_pool_bytes), 0 if none   */
+    uint64_t gather_pool_bytes;
 } bsp_plan_info;
 
 /* Number of persistent CTAs the attention kernel of `mode` wants on `device`
@@ -333,22 +353,30 @@ int bsp_merge_state(const void *o_a, const float *lse_a, const void *o_b, const 
 /*
  * Decode run without any device allocation by the caller or the library.
  *
- * No counterpart on the pages: this is a convenience of this library. It is
- * for callers that cannot call cudaMalloc where they run attention, such as a
- * host framework that has handed all device memory to its own pool and
- * forbids allocation while serving, or code running inside a stream capture
- * in global mode. The caller plans as usual (bsp_plan, where `workspace` may
- * be NULL for a host-only plan) and passes the plan and its staging image;
- * this call copies the plan into a fixed device array owned by the library,
- * uses that array as the workspace (plan metadata and partial states), runs
- * the decode kernel and the merge of partials, and allocates nothing.
+ * The paper has no counterpart: this is a convenience of this library. It is
+ * for callers that cannot call cudaMalloc where they run attention: a serving
+ * engine whose KV-cache manager reserved nearly all of HBM for its own pool
+ * and forbids further allocation while serving, or a plugin that its host
+ * hands only input and output tensors, with no allocator for scratch. The
+ * caller plans as usual (bsp_plan, where `workspace` may be NULL for a
+ * host-only plan) and passes the plan and its staging image; this call copies
+ * the plan into a fixed device array owned by the library, uses that array
+ * as the workspace (plan metadata and partial states), runs the decode kernel
+ * with its merge of split outputs, and allocates nothing.
  *
  *   plan          from bsp_plan, mode BSP_MODE_DECODE; its workspace_bytes
  *                 must not exceed BSP_STATIC_WORKSPACE_BYTES (else
- *                 BSP_ERR_CAPACITY: lower capacity.num_ctas or max_batch)
- *   host_staging  the staging buffer that bsp_plan wrote this plan into
+ *                 BSP_ERR_CAPACITY: lower capacity.num_ctas or max_batch);
+ *                 counts and offsets that do not match the layout of its
+ *                 problem and capacity are BSP_ERR_INVALID_ARG
+ *   host_staging  the staging buffer that bsp_plan wrote this plan into; the
+ *                 copies out of it are queued on `stream`, so it must stay
+ *                 unchanged until they have run (pinned memory makes them
+ *                 asynchronous; pageable memory is copied before return)
  *   other arguments as in bsp_decode_run (device pointers, caller-owned);
- *   the pool size is not passed, so pages are gathered with cp.async.
+ *   the pool size is not passed, so pages are gathered with cp.async, and
+ *   the result is bit for bit that of bsp_decode_run with num_pages = 0 on
+ *   the same plan.
  *
  * The array (BSP_STATIC_WORKSPACE_BYTES of device memory) exists once per
  * device in every process that loads the library and lives until the
@@ -376,7 +404,11 @@ int bsp_check_bounded_wait(int64_t limit_cycles, int32_t *status, bsp_stream_t s
 /* Read (and clear) the device error word that kernels set when a bounded wait
  * gives up or a bounds check trips (it lives in the workspace section at
  * plan->off_status). Synchronises `stream`. *word_out = 0 when clean;
- * otherwise it holds the code of the first check that tripped. */
+ * otherwise it holds the code of the first check that tripped, and the
+ * arrival counts of the plan's reduction map (bsp_merge_entry.arrived, which
+ * CTAs that gave up may have left part-way) are reset to 0 as well, so the
+ * same plan in the same workspace can run again. Outputs of the failed run
+ * are undefined. */
 int bsp_check_device_error(const bsp_plan_info *plan, void *workspace, bsp_stream_t stream,
                            int32_t *word_out);
 

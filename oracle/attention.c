@@ -107,12 +107,14 @@ int oracle_attention_rows(int32_t batch, int32_t H_qo, int32_t H_kv, int32_t D,
         return ORACLE_BAD_INPUT;
     const int32_t g = H_qo / H_kv;
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
+    /* a thread count for this call only (omp_set_num_threads would outlive it) */
+    const int n_threads = num_threads > 0 ? num_threads : omp_get_max_threads();
 #else
+    const int n_threads = 1;
     (void)num_threads;
 #endif
     int bad = 0;
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad) num_threads(n_threads)
     for (int64_t s = 0; s < n_sel; ++s) {
         const int64_t tok = sel_token[s];
         const int32_t h = sel_head[s];

@@ -46,8 +46,9 @@ def test_struct_layout_matches_header(native, tmp_path):
 int main(void) {
   printf("%zu %zu %zu %zu %zu\n", sizeof(bsp_problem), sizeof(bsp_capacity), sizeof(bsp_plan_info),
          sizeof(bsp_work_item), sizeof(bsp_merge_entry));
-  printf("%zu %zu %zu %zu\n", offsetof(bsp_plan_info, total_work), offsetof(bsp_plan_info, off_header),
-         offsetof(bsp_plan_info, off_partial_o), offsetof(bsp_plan_info, valid));
+  printf("%zu %zu %zu %zu %zu %zu\n", offsetof(bsp_plan_info, total_work), offsetof(bsp_plan_info, off_header),
+         offsetof(bsp_plan_info, off_partial_o), offsetof(bsp_plan_info, valid),
+         offsetof(bsp_plan_info, off_gather), offsetof(bsp_capacity, max_gather_pages));
   return 0;
 }''')
     exe = tmp_path / "sizes"
@@ -58,7 +59,8 @@ int main(void) {
     assert [int(x) for x in sizes.split()] == want
     PI = native.PlanInfo
     assert [int(x) for x in offs.split()] == [PI.total_work.offset, PI.off_header.offset, PI.off_partial_o.offset,
-                                              PI.valid.offset]
+                                              PI.valid.offset, PI.off_gather.offset,
+                                              native.Capacity.max_gather_pages.offset]
 
 
 def test_version_and_error_strings(native):
@@ -97,3 +99,31 @@ def test_bounded_wait_self_test_rejects_bad_arguments(native):
     assert lib.bsp_check_bounded_wait(1000, None, None) == native.BSP_ERR_INVALID_ARG
     assert lib.bsp_check_bounded_wait(0, ctypes.c_void_p(16), None) == native.BSP_ERR_INVALID_ARG
     assert lib.bsp_check_bounded_wait(1 << 34, ctypes.c_void_p(16), None) == native.BSP_ERR_INVALID_ARG
+
+
+def test_gather_region_in_the_workspace(native):
+    """capacity.max_gather_pages (prefill) adds a K and a V region of that many
+    pages to the workspace, after the partial states; the plan reports where,
+    and how many pages its table has. Decode rejects a region."""
+    import numpy as np
+    lib = native.load()
+    pre = native.Problem(1, 32, 8, 128, 1, 1, 0)
+    base = lib.bsp_workspace_size(ctypes.byref(pre), ctypes.byref(native.Capacity(2, 16, 4096, 1, 0)))
+    pages = 5000
+    ws = lib.bsp_workspace_size(ctypes.byref(pre), ctypes.byref(native.Capacity(2, 16, 4096, 1, pages)))
+    pool = -(-pages * 1 * 8 * 128 * 2 // 256) * 256
+    assert ws == base + 2 * pool
+    cap = native.Capacity(2, 16, 4096, 1, pages)
+    staging = np.zeros(lib.bsp_host_staging_size(ctypes.byref(pre), ctypes.byref(cap)), np.uint8)
+    qo = np.array([0, 100, 300], np.int32)
+    kv = np.array([0, 700, 2000], np.int32)
+    lp = np.ones(2, np.int32)
+    info = native.PlanInfo()
+    native.check(lib.bsp_plan(ctypes.byref(pre), ctypes.byref(cap), 2, qo.ctypes.data_as(ctypes.c_void_p),
+                              kv.ctypes.data_as(ctypes.c_void_p), lp.ctypes.data_as(ctypes.c_void_p), 2, 1,
+                              staging.ctypes.data_as(ctypes.c_void_p), None, 0, None, ctypes.byref(info)))
+    assert info.num_table_pages == 2000 and info.gather_pool_bytes == pool
+    assert info.off_gather == info.workspace_bytes - 2 * pool and info.off_gather % 256 == 0
+    dec = native.Problem(0, 32, 8, 128, 1, 0, 0)
+    assert lib.bsp_workspace_size(ctypes.byref(dec), ctypes.byref(native.Capacity(2, 16, 2, 1, 10))) == 0
+    assert b"max_gather_pages" in lib.bsp_last_error()

@@ -9,7 +9,7 @@ import torch
 import oracle
 import workloads
 from block_sparse_paged_gb300 import _native as N
-from gpu_helpers import (compare, lib, oracle_full, run_batch, sample_rows, to_dev)
+from gpu_helpers import (compare, lib, oracle_full, run_batch, timed, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,12 +59,11 @@ def test_random_bf16_decode(bsp, case):
 
 def test_batched_decode_full_size(bsp):
     """Llama-3-8B-shaped batch at full size (64 requests, KV U{512..8192}, page
-    16), sampled rows against the oracle, with the bench's CTA count."""
+    16), every output row against the oracle, with the bench's CTA count."""
     b = workloads.batched_decode_bf16()
     out, lse, pa = run_batch(bsp, b)
-    tok, head = sample_rows(b, 256, 11)
-    O, L = oracle.attention_rows_of(b, tok, head)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, b)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
     # run twice: bitwise identical (fixed plan, fixed reduction order)
     q, k, v, idx = to_dev(b)
     out2, lse2 = pa.run(q, k, v, idx, b.sm_scale)
@@ -74,14 +73,14 @@ def test_batched_decode_full_size(bsp):
 
 def test_vector_sparse_permuted_equals_contiguous(bsp):
     """Page size 1, every slot permuted, 64/8 heads: the permuted and the
-    contiguous layouts give bitwise-equal outputs; sampled rows match the oracle."""
+    contiguous layouts give bitwise-equal outputs; every output row matches the
+    oracle."""
     perm, cont = workloads.vector_sparse_decode_bf16()
     out_p, lse_p, _ = run_batch(bsp, perm)
     out_c, lse_c, _ = run_batch(bsp, cont)
     assert torch.equal(out_p, out_c) and torch.equal(lse_p, lse_c)
-    tok, head = sample_rows(perm, 128, 12)
-    O, L = oracle.attention_rows_of(perm, tok, head)
-    compare(out_p, lse_p, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, perm)
+    compare(out_p, lse_p, O, L, "bf16", oracle_s=t)
 
 
 @pytest.mark.parametrize("ps,D", [(16, 128), (8, 64), (64, 128)])
@@ -127,12 +126,11 @@ def test_many_slot_folds(bsp, dtype):
 
 def test_shared_prefix_full_view_decode(bsp):
     """The shared-prefix batch read without composition (every request over
-    prefix + suffix pages), including the 32768-token outlier; sampled rows."""
+    prefix + suffix pages), including the 32768-token outlier; every output row."""
     sp = workloads.shared_prefix_decode_bf16()
     out, lse, _ = run_batch(bsp, sp.full)
-    tok, head = sample_rows(sp.full, 128, 13)
-    O, L = oracle.attention_rows_of(sp.full, tok, head)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, sp.full)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
 
 
 def test_cuda_graph_replay_with_new_plan(bsp):
@@ -227,6 +225,33 @@ def test_merge_state_arbitrary_states(bsp, dtype):
     bsp.merge_state(a_dev, la_dev, tb.cuda(), torch.from_numpy(lb).cuda(), out=a_dev, lse_out=la_dev)
     torch.cuda.synchronize()
     assert torch.equal(a_dev, out) and torch.equal(la_dev, lse)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_merge_state_unaligned_rows(bsp, dtype):
+    """O arrays that start one element past an aligned address take the
+    element-wise path of merge_state; its results equal the vector path's bit
+    for bit."""
+    rng = np.random.default_rng(32)
+    n, H, D = 77, 8, 128
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    oa = torch.from_numpy(rng.standard_normal((n, H, D)).astype(np.float32)).to(t).cuda()
+    ob = torch.from_numpy(rng.standard_normal((n, H, D)).astype(np.float32)).to(t).cuda()
+    la = torch.from_numpy((rng.standard_normal((n, H)) * 3).astype(np.float32)).cuda()
+    lb = torch.from_numpy((rng.standard_normal((n, H)) * 3).astype(np.float32)).cuda()
+    ref_o, ref_l = bsp.merge_state(oa, la, ob, lb)
+
+    def shifted(x):
+        buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=x.device)
+        v = buf[1:].view(x.shape)
+        v.copy_(x)
+        return v
+    ua, ub = shifted(oa), shifted(ob)
+    uo = shifted(torch.empty_like(oa))
+    assert ua.data_ptr() % 8 != 0
+    out, lse = bsp.merge_state(ua, la, ub, lb, out=uo)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
 
 
 def test_run_rejects_bad_arguments(bsp):

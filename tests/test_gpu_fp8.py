@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import compare, lib, sample_rows
+from gpu_helpers import compare, lib, timed
 
 pytestmark = pytest.mark.gpu
 
@@ -88,17 +88,14 @@ def test_fp8_scales_are_applied(bsp):
 
 def test_fp8_full_size_decode(bsp):
     """The Llama-3-8B-shaped batched decode (batch 64, KV up to 8192, page 16)
-    with e4m3 K / V: sampled rows against the oracle; run twice on one plan
+    with e4m3 K / V: every output row against the oracle; run twice on one plan
     (the in-kernel merge resets its counters)."""
     b = workloads.batched_decode_bf16()
     f8 = workloads.fp8_kv(b)
     out, lse, pa = run_fp8(bsp, b, f8, repeats=2)
-    tok, head = sample_rows(b, 256, 31)
-    kd = oracle.fp8.dequantize(f8.k8.numpy(), f8.k_scale).astype(np.float32)
-    vd = oracle.fp8.dequantize(f8.v8.numpy(), f8.v_scale).astype(np.float32)
-    # float32 copies of the fp64 values: e4m3 * scale rounds once, far below the bounds
-    O, L = oracle.attention_rows_of(b, tok, head, k_f32=kd, v_f32=vd)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    kd, vd = oracle_kv(f8)
+    (O, L), t = timed(oracle.attention_of, b, k=kd, v=vd)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
     assert pa.check_device_error() == 0
 
 

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import compare, lib, oracle_full, run_batch, sample_rows, to_dev
+from gpu_helpers import compare, lib, oracle_full, run_batch, stratified_rows, timed, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -124,12 +124,11 @@ def test_prefill_cuda_graph_replay_with_new_plan(bsp):
 
 def test_ragged_causal_prefill_full_size(bsp):
     """16 requests, qo = kv ~ U{128..2048}, page 16 permuted, 32/8 heads, causal;
-    sampled rows against the oracle; two runs bitwise equal."""
+    every output row against the oracle; two runs bitwise equal."""
     b = workloads.ragged_causal_prefill_bf16()
     out, lse, pa = run_batch(bsp, b, mode="prefill")
-    tok, head = sample_rows(b, 384, 21)
-    O, L = oracle.attention_rows_of(b, tok, head)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, b)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
     q, k, v, idx = to_dev(b)
     out2, lse2 = pa.run(q, k, v, idx, b.sm_scale)
     torch.cuda.synchronize()
@@ -225,17 +224,16 @@ def test_shared_prefix_concurrent_views(bsp):
 def test_shared_prefix_composable_full_size(bsp):
     """64 requests sharing an 8192-token prefix, suffixes U{64..1024} and one
     32768 outlier: prefix view + suffix view + merge equals attention over the
-    full page lists (sampled rows)."""
+    full page lists (every output row)."""
     sp = workloads.shared_prefix_decode_bf16()
     out, lse = composable_decode(bsp, sp)
-    tok, head = sample_rows(sp.full, 256, 22)
-    O, L = oracle.attention_rows_of(sp.full, tok, head)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, sp.full)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
     # the bench's split: 32 CTAs for the prefix view (4 equal chunks per tile),
     # the rest for the suffix view
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     out2, lse2 = composable_decode(bsp, sp, num_ctas_prefill=32, num_ctas_decode=sms - 32)
-    compare(out2, lse2, O, L, "bf16", rows=(tok, head))
+    compare(out2, lse2, O, L, "bf16")
 
 
 def test_vector_sparse_prefill_small(bsp):
@@ -252,12 +250,77 @@ def test_vector_sparse_prefill_small(bsp):
 
 def test_vector_sparse_prefill_full_size(bsp):
     """Page size 1, one 32768-token causal prefill (the long vector-sparse
-    prefill): sampled rows against the oracle, permuted == contiguous bitwise."""
+    prefill) in the bench's configuration (a gather region for the whole page
+    table, the default CTA count): a stratified eighth of the rows against the
+    oracle (every head, every 8th position with a seeded phase per head, all of
+    the first and last query tile; the whole would be ~5 min of fp64 on 16
+    cores); permuted == contiguous bitwise, and both equal the cp.async gather
+    without a region."""
     perm, cont = workloads.vector_sparse_prefill_bf16()
-    o1, l1, pa = run_batch(bsp, perm, mode="prefill")
-    tok, head = sample_rows(perm, 192, 23)
-    O, L = oracle.attention_rows_of(perm, tok, head)
-    compare(o1, l1, O, L, "bf16", rows=(tok, head))
+    n = int(perm.kv_indptr[-1])
+    o1, l1, pa = run_batch(bsp, perm, mode="prefill", max_gather_pages=n)
+    tok, head = stratified_rows(perm, 8, 23)
+    (O, L), t = timed(oracle.attention_rows_of, perm, tok, head)
+    compare(o1, l1, O, L, "bf16", rows=(tok, head), oracle_s=t)
     assert pa.check_device_error() == 0
-    o2, l2, _ = run_batch(bsp, cont, mode="prefill")
+    del pa
+    o2, l2, _ = run_batch(bsp, cont, mode="prefill", max_gather_pages=n)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o3, l3, _ = run_batch(bsp, perm, mode="prefill")
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+GATHER = [
+    # (seed, qo lens, kv lens, H_qo, H_kv, page, causal, num_ctas)
+    (131, [65, 300, 17], [65, 300, 17], 32, 8, 1, True, 11),
+    (132, [140, 33], [400, 33], 16, 4, 2, True, 6),
+    (133, [96, 250, 1], [700, 250, 0], 32, 8, 3, True, 40),      # splits + merges, an empty request
+    (134, [200, 90], [900, 90], 32, 8, 12, False, 9),           # 12-token pages (not a power of two)
+]
+
+
+@pytest.mark.parametrize("case", GATHER, ids=[f"gather{c[0]}" for c in GATHER])
+def test_gathered_prefill_equals_cp_async(bsp, case):
+    """Pages the TMA page gather cannot take (under 8 tokens, or not a power of
+    two) with a gather region in the workspace: the page table's pages are
+    copied into it in table order and read back by 128-row TMA boxes. Same plan
+    and the same shared-memory tiles as the cp.async gather, so the outputs are
+    bitwise equal to it; against the oracle. A region one page too small runs
+    the cp.async gather."""
+    seed, qo, kv, hq, hk, ps, causal, C = case
+    b = workloads.paged_batch(seed, qo, kv, hq, hk, 128, ps, "bf16", causal=causal, extra_pages=3)
+    n = int(b.kv_indptr[-1])
+    dev = to_dev(b)
+    o0, l0, _ = run_batch(bsp, b, mode="prefill", num_ctas=C, dev_tensors=dev)
+    o1, l1, pa = run_batch(bsp, b, mode="prefill", num_ctas=C, dev_tensors=dev, max_gather_pages=n)
+    assert pa.info.off_gather > 0 and pa.info.num_table_pages == n
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert pa.check_device_error() == 0
+    O, L = oracle_full(b)
+    compare(o1, l1, O, L, "bf16")
+    o2, l2, _ = run_batch(bsp, b, mode="prefill", num_ctas=C, dev_tensors=dev, max_gather_pages=max(1, n - 1))
+    assert torch.equal(o0, o2) and torch.equal(l0, l2)
+
+
+def test_gathered_prefill_variants_and_sink(bsp):
+    """The gathered path with a sliding window, a soft-cap and sinks (the
+    variant kernel), page size 1; against the oracle."""
+    b = workloads.paged_batch(135, [200, 90], [700, 90], 16, 4, 128, 1, "bf16", causal=True, extra_pages=2)
+    b.window_left, b.soft_cap = 77, 2.5
+    sk = np.random.default_rng(135).uniform(-2.0, 4.0, size=16)
+    O, L = oracle_full(b, sink=sk)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=7, sink=sk, max_gather_pages=int(b.kv_indptr[-1]))
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
+def test_gather_reports_page_ids_out_of_range(bsp):
+    """The gather checks every page id against the pool size: an id outside it
+    gives a zero page and the status word 0x301 (no out-of-range read)."""
+    b = workloads.paged_batch(136, [50, 40], [50, 40], 32, 8, 128, 1, "bf16", causal=True, extra_pages=2)
+    q, k, v, idx = to_dev(b)
+    idx[3] = k.shape[0] + 5
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=4, dev_tensors=(q, k, v, idx),
+                             max_gather_pages=int(b.kv_indptr[-1]))
+    assert pa.check_device_error() == 0x301
+    assert pa.check_device_error() == 0

@@ -5,9 +5,8 @@ inputs."""
 import numpy as np
 import pytest
 
-import oracle
 import workloads
-from gpu_helpers import compare, lib, oracle_full, run_batch, sample_rows
+from gpu_helpers import compare, lib, oracle_full, run_batch, timed
 
 pytestmark = pytest.mark.gpu
 
@@ -63,12 +62,11 @@ def test_prefill_variants(bsp, case):
 
 def test_prefill_window_full_size(bsp):
     """The ragged causal prefill workload with a 512-token window and a soft-cap
-    of 30: sampled rows against the oracle."""
+    of 30: every output row against the oracle."""
     b = with_variant(workloads.ragged_causal_prefill_bf16(), 512, 30.0)
     out, lse, pa = run_batch(bsp, b, mode="prefill")
-    tok, head = sample_rows(b, 256, 25)
-    O, L = oracle.attention_rows_of(b, tok, head)
-    compare(out, lse, O, L, "bf16", rows=(tok, head))
+    (O, L), t = timed(oracle_full, b)
+    compare(out, lse, O, L, "bf16", oracle_s=t)
 
 
 def sinks(h, seed):

@@ -73,3 +73,16 @@ def test_pins_catch_planted_mistake(name, old, new, tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode != 3, f"no pin caught the planted mistake {name}"
     assert r.returncode == 0 or r.returncode < 0, r.stderr[-2000:]
+
+
+def test_thread_count_applies_to_one_call_only():
+    """A call with an explicit thread count leaves the default for later calls
+    (all available threads) unchanged, and the result does not depend on it."""
+    import numpy as np
+    import workloads
+    b = workloads.paged_batch(5, [1, 1, 1], [100, 300, 7], 8, 2, 64, 16, "bf16")
+    n = oracle.num_threads_available()
+    O1, L1 = oracle.attention_of(b, num_threads=1)
+    assert oracle.num_threads_available() == n
+    O2, L2 = oracle.attention_of(b)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
