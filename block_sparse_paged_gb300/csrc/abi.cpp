@@ -25,6 +25,15 @@ void clear_error() {
 
 int last_code() { return g_code == BSP_OK ? BSP_ERR_INVALID_ARG : g_code; }
 
+int check_aligned16(const void *q, const void *k, const void *v, const void *o, const void *workspace) {
+    const void *ptr[5] = {q, k, v, o, workspace};
+    const char *name[5] = {"q", "k_pages", "v_pages", "o", "workspace"};
+    for (int i = 0; i < 5; ++i)
+        if (reinterpret_cast<uintptr_t>(ptr[i]) % 16 != 0)
+            return fail(BSP_ERR_INVALID_ARG, std::string(name[i]) + " is not 16-byte aligned");
+    return BSP_OK;
+}
+
 namespace {
 
 int check_plan(const bsp_plan_info *plan, int mode, const void *workspace) {
@@ -69,6 +78,7 @@ extern "C" int bsp_decode_run(const bsp_plan_info *plan, const void *q, const vo
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (num_pages < 0) return fail(BSP_ERR_INVALID_ARG, "num_pages must not be negative");
+    if ((rc = check_aligned16(q, k_pages, v_pages, o, workspace)) != BSP_OK) return rc;
     // split outputs are merged inside the decode kernel (by the CTA that writes
     // an output's last partial state): one launch
     return launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
@@ -82,6 +92,7 @@ extern "C" int bsp_decode_run_fp8(const bsp_plan_info *plan, const void *q, cons
     int rc = check_plan(plan, BSP_MODE_DECODE, workspace);
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if ((rc = check_aligned16(q, k_pages, v_pages, o, workspace)) != BSP_OK) return rc;
     return launch_decode_fp8(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, k_scale, v_scale, o, lse,
                              workspace, stream);
 }
@@ -94,6 +105,7 @@ extern "C" int bsp_prefill_run(const bsp_plan_info *plan, const void *q, const v
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
     if (num_pages < 1) return fail(BSP_ERR_INVALID_ARG, "num_pages must be positive");
+    if ((rc = check_aligned16(q, k_pages, v_pages, o, workspace)) != BSP_OK) return rc;
     rc = launch_prefill(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);
     if (rc != BSP_OK) return rc;
     return launch_reduce(plan, o, lse, workspace, stream);
@@ -108,6 +120,7 @@ extern "C" int bsp_run_attention(const bsp_plan_info *plan, const void *q, const
     int rc = check_plan(plan, mode, workspace);
     if (rc != BSP_OK) return rc;
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if ((rc = check_aligned16(q, k_pages, v_pages, o, workspace)) != BSP_OK) return rc;
     if (mode == BSP_MODE_DECODE) {
         if (num_pages < 0) return fail(BSP_ERR_INVALID_ARG, "num_pages must not be negative");
         return launch_decode(plan, q, k_pages, v_pages, kv_indices, num_pages, sm_scale, o, lse, workspace, stream);

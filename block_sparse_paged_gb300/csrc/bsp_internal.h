@@ -56,6 +56,11 @@ int last_code();
 
 inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
+// The run kernels move q, K / V rows, o and the workspace's partial states in
+// 16-byte units: BSP_OK, or BSP_ERR_INVALID_ARG naming the first pointer that
+// is not 16-byte aligned.
+int check_aligned16(const void *q, const void *k, const void *v, const void *o, const void *workspace);
+
 // 3-D bf16 TMA map over a [rows][heads][dim] array (dim a multiple of 64):
 // boxes of 64 elements x box_heads x box_rows, 128-byte swizzle. BSP_OK or
 // BSP_ERR_* (unaligned base, encoder unavailable or rejecting the shape).

@@ -66,6 +66,8 @@ constexpr int kConsumers = 4;
 constexpr int kTileK = 64;                   // unit of the stage sizes below; the largest page box (rows)
 constexpr int kStages = 5;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at 2 GHz: a fault, not a stall
+// reduction-map entries a CTA completes and folds after its queue (more are folded at once)
+constexpr int kMaxPendingFolds = 32;
 
 // Four e4m3 values (the bytes of x, lowest first) to two f16x2: lo = bytes 0
 // and 1, hi = bytes 2 and 3, the lower byte in the lower half. Exact: every
@@ -121,9 +123,12 @@ struct DecodeLayout {
     static constexpr int kScratchOff = kRingBytes;
     static constexpr int kScratchBytes = kCons * kScrRows * D * 4;   // per-warp O rows for the item merge
     static constexpr int kStatBytes = kCons * kScrRows * 2 * 4;      // per-warp (m, l)
-    static constexpr int kBarOff = kScratchOff + kScratchBytes + kStatBytes;
-    static constexpr int kNumBars = 2 * kS + 3;             // full[S], empty[S], merge_in, merge_out, last
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
+    static constexpr int kFacBytes = (kCons + 1) * kScrRows * 4;     // per-(warp, row) weights, per-row LSE
+    static constexpr int kBarOff = kScratchOff + kScratchBytes + kStatBytes + kFacBytes;
+    static constexpr int kNumBars = 2 * kS + 3;             // full[S], empty[S], merge_in, merge_mid, merge_out
+    // after the barriers: abort flag, pending-fold count and list
+    static constexpr int kFlagBytes = 8 + 4 * (1 + kMaxPendingFolds);
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + kFlagBytes + (kTma ? 1024 : 0);  // TMA: 1024-byte alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "decode ring exceeds shared memory");
     // byte offset of 16-byte chunk c (of D / 8) of ring row r inside a K or V tile
     __device__ static __forceinline__ uint32_t chunk(int r, int c) {
@@ -279,9 +284,10 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
 
     const uint32_t sbase = smem_u32(smem);  // 1024-byte aligned in the TMA layout
     const uint32_t full0 = sbase + LY::kBarOff, empty0 = full0 + kStages * 8;
-    const uint32_t merge_in = empty0 + kStages * 8, merge_out = merge_in + 8, last_bar = merge_out + 8;
+    const uint32_t merge_in = empty0 + kStages * 8, merge_mid = merge_in + 8, merge_out = merge_mid + 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + LY::kBarOff + LY::kNumBars * 8);
-    volatile int *last_flag = abort_flag + 1;  // "this CTA wrote an output's last partial"
+    // entries whose count this CTA completed: [0] how many, then their indices
+    volatile int *pending = abort_flag + 2;
 
     // Rows past a chunk's end are never copied: zero the ring once so that
     // they hold finite values (their probabilities are exactly 0).
@@ -293,9 +299,10 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             sm100::mbar_init(empty0 + 8 * s, kConsumers);
         }
         sm100::mbar_init(merge_in, kConsumers);
+        sm100::mbar_init(merge_mid, kConsumers);
         sm100::mbar_init(merge_out, kConsumers);
-        sm100::mbar_init(last_bar, 1);
         *abort_flag = 0;
+        pending[0] = 0;
         sm100::fence_barrier_init();
     }
     if (kTma && warp == kConsumers && lane == 0) {
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     const int r0 = lane >> 2, r1 = r0 + 8;
     float *scratch = reinterpret_cast<float *>(smem + LY::kScratchOff);                      // [warp][16][D]
     float *stats = reinterpret_cast<float *>(smem + LY::kScratchOff + LY::kScratchBytes);  // [warp][16][m, l]
-    int k = 0, merges = 0, lasts = 0;
+    int k = 0, merges = 0;
     bsp_merge_entry *mmap = reinterpret_cast<bsp_merge_entry *>(const_cast<uint8_t *>(p.ws) + p.off_merges);
     bsp_work_item w_next = items[it0];
     for (int it = it0; it < it1; ++it) {
@@ -768,57 +775,92 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(merge_in);
         if (!__all_sync(0xffffffffu, wait_or_abort(merge_in, merges & 1, abort_flag, status, kStatusMergeWait))) return;
-        for (int e = warp * 32 + lane; e < g * D; e += kConsumers * 32) {
-            const int row = e / D, d = e - row * D;
+        // Combination weights, once per row: warp ww's state of row r enters as
+        // fac[ww][r] = 2^(m_ww - M) / L (times the output scale, and the sink's
+        // factor for a final row); rlse[r] is the row's LSE.
+        float *fac = stats + kConsumers * kSR * 2;  // [warp][row]
+        float *rlse = fac + kConsumers * kSR;       // [row]
+        const int ct = warp * 32 + lane;
+        if (ct < g) {
             float M = -INFINITY;
 #pragma unroll
-            for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, stats[(ww * kSR + row) * 2]);
-            float val = 0.f, lse_v = -INFINITY;
-            if (M != -INFINITY) {
-                float L = 0.f, num = 0.f;
+            for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, stats[(ww * kSR + ct) * 2]);
+            float f[kConsumers], L = 0.f;
 #pragma unroll
-                for (int ww = 0; ww < kConsumers; ++ww) {
-                    const float f = exp2f(stats[(ww * kSR + row) * 2] - M);
-                    L += stats[(ww * kSR + row) * 2 + 1] * f;
-                    num += scratch[(ww * kSR + row) * D + d] * f;
-                }
-                val = num / L * p.v_scale;
-                lse_v = (M + log2f(L)) * kLn2;
+            for (int ww = 0; ww < kConsumers; ++ww) {
+                f[ww] = M != -INFINITY ? exp2f(stats[(ww * kSR + ct) * 2] - M) : 0.f;
+                L += stats[(ww * kSR + ct) * 2 + 1] * f[ww];
+            }
+            float inv = M != -INFINITY ? p.v_scale / L : 0.f;
+            float lse_v = M != -INFINITY ? (M + log2f(L)) * kLn2 : -INFINITY;
+            if (w.slot < 0 && p.sink) inv *= fold_sink(lse_v, p.sink[w.kv_head * g + ct]);
+#pragma unroll
+            for (int ww = 0; ww < kConsumers; ++ww) fac[ww * kSR + ct] = f[ww] * inv;
+            rlse[ct] = lse_v;
+        }
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(merge_mid);
+        if (!__all_sync(0xffffffffu, wait_or_abort(merge_mid, merges & 1, abort_flag, status, kStatusMergeWait))) return;
+        // one (row, 4 columns) unit per thread and pass: the warps' float4s
+        // weighted and summed, then 4 bf16 of the output or a float4 of the partial
+        for (int u = ct; u < g * (D / 4); u += kConsumers * 32) {
+            const int row = u / (D / 4), cq = u - row * (D / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int ww = 0; ww < kConsumers; ++ww) {
+                const float fw = fac[ww * kSR + row];
+                const float4 x = reinterpret_cast<const float4 *>(scratch + (ww * kSR + row) * D)[cq];
+                acc.x = fmaf(fw, x.x, acc.x);
+                acc.y = fmaf(fw, x.y, acc.y);
+                acc.z = fmaf(fw, x.z, acc.z);
+                acc.w = fmaf(fw, x.w, acc.w);
             }
             if (w.slot < 0) {
                 const size_t orow = (size_t)w.q_tok0 * p.H_qo + (size_t)w.kv_head * g + row;
-                if (p.sink) val *= fold_sink(lse_v, p.sink[w.kv_head * g + row]);
-                static_cast<__nv_bfloat16 *>(p.o)[orow * D + d] = __float2bfloat16_rn(val);
-                if (d == 0 && p.lse) p.lse[orow] = lse_v;
+                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.o) + orow * D + cq * 4) =
+                    make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+                if (cq == 0 && p.lse) p.lse[orow] = rlse[row];
             } else {
                 const size_t prow = (size_t)w.slot * p.tile_rows + row;
-                reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_po)[prow * D + d] = val;
-                if (d == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = lse_v;
+                reinterpret_cast<float4 *>(const_cast<uint8_t *>(p.ws) + p.off_po)[prow * (D / 4) + cq] = acc;
+                if (cq == 0) reinterpret_cast<float *>(const_cast<uint8_t *>(p.ws) + p.off_plse)[prow] = rlse[row];
             }
         }
-        if (w.slot >= 0) __threadfence();  // this thread's partial rows, before the arrival count below
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(merge_out);
         if (!__all_sync(0xffffffffu, wait_or_abort(merge_out, merges & 1, abort_flag, status, kStatusMergeWait))) return;
         ++merges;
-        if (w.slot >= 0) {
-            // Split output: count this partial in the reduction-map entry; the CTA
-            // whose partial completes the count merges all of them (nobody waits
-            // for another CTA, so no wait can depend on scheduling).
-            if (warp == 0 && lane == 0) {
-                const int prev = atomicAdd(&mmap[w.merge].arrived, 1);
-                *last_flag = prev == mmap[w.merge].n_slots - 1;
-                sm100::mbar_arrive(last_bar);
-            }
-            if (!__all_sync(0xffffffffu, wait_or_abort(last_bar, lasts & 1, abort_flag, status, kStatusMergeWait))) return;
-            ++lasts;
-            if (*last_flag) {
-                __threadfence();
-                const bsp_merge_entry e = mmap[w.merge];
-                merge_entry<D, __nv_bfloat16>(p, e, warp * 32 + lane, kConsumers * 32);
-                if (warp == 0 && lane == 0) mmap[w.merge].arrived = 0;  // ready for the next run of the plan
+        if (w.slot >= 0 && warp == 0 && lane == 0) {
+            // Split output: count this partial in its reduction-map entry. Every
+            // consumer thread wrote its partial rows before merge_out; one gpu-scope
+            // fence here orders them all (fences are cumulative) before the count.
+            // The CTA whose partial completes the count folds the entry after its
+            // queue (nobody waits for another CTA, and no warp waits here for the
+            // atomic's round trip).
+            __threadfence();
+            const int prev = atomicAdd(&mmap[w.merge].arrived, 1);
+            if (prev == mmap[w.merge].n_slots - 1) {
+                __threadfence();  // acquire: the other CTAs' partials, counted before their arrivals
+                const int n = pending[0];
+                if (n < kMaxPendingFolds) {
+                    pending[1 + n] = w.merge;
+                    pending[0] = n + 1;
+                } else {  // list full: fold this entry now, by this thread alone
+                    merge_entry<D, __nv_bfloat16>(p, mmap[w.merge], 0, 1);
+                    mmap[w.merge].arrived = 0;  // ready for the next run of the plan
+                }
             }
         }
+    }
+    // ---- folds of the entries this CTA completed ----------------------------
+    __syncwarp();
+    if (lane == 0) sm100::mbar_arrive(merge_in);
+    if (!__all_sync(0xffffffffu, wait_or_abort(merge_in, merges & 1, abort_flag, status, kStatusMergeWait))) return;
+    const int n_pending = pending[0];
+    for (int i = 0; i < n_pending; ++i) {
+        const int ei = pending[1 + i];
+        merge_entry<D, __nv_bfloat16>(p, mmap[ei], warp * 32 + lane, kConsumers * 32);
+        if (warp == 0 && lane == 0) mmap[ei].arrived = 0;  // ready for the next run of the plan
     }
 }
 

@@ -60,6 +60,7 @@ extern "C" int bsp_decode_run_static(const bsp_plan_info *plan, const void *host
     if (plan->problem.mode != BSP_MODE_DECODE) return fail(BSP_ERR_INVALID_ARG, "plan was made for prefill, not decode");
     if (!host_staging) return fail(BSP_ERR_INVALID_ARG, "host_staging (the plan's staging image) is NULL");
     if (!q || !k_pages || !v_pages || !o) return fail(BSP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (check_aligned16(q, k_pages, v_pages, o, nullptr) != BSP_OK) return last_code();
     Layout l;
     if (!compute_layout(&plan->problem, &plan->capacity, &l)) return last_code();
     if (l.total != plan->workspace_bytes || l.off_partial_o != plan->off_partial_o)

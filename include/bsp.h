@@ -43,7 +43,8 @@
  *   - Every pointer is owned by the caller. Device pointers are plain CUDA
  *     device addresses of the current device; host pointers are plain host
  *     memory. No entry point allocates device memory; bsp_plan allocates only
- *     small host scratch.
+ *     small host scratch. The run calls take q, k_pages, v_pages, o and the
+ *     workspace 16-byte aligned (BSP_ERR_INVALID_ARG otherwise).
  *   - Layouts (row-major, innermost last):
  *       q, o          [n_tokens, H_qo, D]      ragged, no padding
  *       lse           [n_tokens, H_qo]         float32, natural log
