@@ -530,14 +530,16 @@ def secondary(bsp, dev, args, pk):
 
 def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0.0):
     """Page size 1 (every token slot permuted) vs the same KV contiguous: GB/s
-    of each and their ratio."""
+    of each and their ratio, under the equal-share schedule (256 equal tiles on
+    152 CTAs: LPT over whole tiles leaves 48 CTAs with half the work), and the
+    permuted layout under the pages' LPT plan for comparison."""
     import workloads
     perm, cont = workloads.vector_sparse_decode_bf16()
     r = {}
-    for tag, b in (("permuted", perm), ("contiguous", cont)):
+    for tag, b, sched in (("permuted", perm, "equal"), ("contiguous", cont, "equal"), ("permuted_lpt", perm, "lpt")):
         C = num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
         pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, 1, False, torch.bfloat16,
-                                max_batch=b.batch, num_ctas=C, device=dev)
+                                max_batch=b.batch, num_ctas=C, device=dev, schedule=sched)
         pa.plan(b.kv_indptr, b.last_page_len)
         q, k, v, idx = to_dev(b, dev)
         out = torch.empty_like(q)
@@ -551,7 +553,7 @@ def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0
         torch.cuda.empty_cache()
     r["permuted_over_contiguous"] = round(r["permuted"]["GB/s"] / r["contiguous"]["GB/s"], 4)
     r["workload"] = ("32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16; "
-                     "one launch per run, 10 per graph replay")
+                     "equal-share plan (permuted_lpt: the pages' LPT plan); one launch per run, 10 per graph replay")
     r["roofline"] = {"bound": "hbm", "kernel": "decode_bf16_kernel<128, cp.async gather>",
                      "achieved": r["permuted"]["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": r["permuted"]["frac_of_hbm"], "peak_source": "measured (STREAM-style copy)",

@@ -22,6 +22,8 @@ BSP_ERR_DEVICE_CHECK = -5
 
 BSP_DTYPE_BF16 = 0
 BSP_DTYPE_F32 = 1
+BSP_SCHEDULE_LPT = 0
+BSP_SCHEDULE_EQUAL_SHARES = 1
 BSP_MODE_DECODE = 0
 BSP_MODE_PREFILL = 1
 BSP_STATIC_WORKSPACE_BYTES = 8 << 20
@@ -44,7 +46,8 @@ class Problem(ctypes.Structure):
 
 class Capacity(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("max_qo_tokens", ctypes.c_int64),
-                ("chunks_per_cta", ctypes.c_int32), ("max_gather_pages", ctypes.c_int32)]
+                ("chunks_per_cta", ctypes.c_int32), ("max_gather_pages", ctypes.c_int32),
+                ("schedule", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -92,6 +92,8 @@ class PagedAttention:
     max_gather_pages (prefill): pages of a K / V copy region in the workspace;
     prefills whose pages are under 8 tokens (or not a power of two) and whose
     page table fits it are gathered into it first and then read by TMA.
+    schedule: "lpt" (the pages' plan) or "equal" (equal contiguous shares of
+    the concatenated KV ranges per CTA, for batches of few, equal tiles).
     The workspace and pinned staging buffer are allocated once, for the
     given bounds; plan() may then be called once per step and run() once per
     layer, and run() can be captured in a CUDA graph.
@@ -101,7 +103,7 @@ class PagedAttention:
                  causal: bool = False, dtype=torch.bfloat16, max_batch: int = 256,
                  max_qo_tokens: int | None = None, num_ctas: int | None = None, device=None,
                  window_left: int = -1, logits_soft_cap: float = 0.0, chunks_per_cta: int = 1,
-                 max_gather_pages: int = 0):
+                 max_gather_pages: int = 0, schedule: str = "lpt"):
         self.lib = N.load()
         if mode not in ("decode", "prefill"):
             raise ValueError("mode must be 'decode' or 'prefill'")
@@ -114,7 +116,10 @@ class PagedAttention:
             num_ctas = default_num_ctas(self.mode, self.device.index)
         if max_qo_tokens is None:
             max_qo_tokens = max_batch if mode == "decode" else 65536
-        self.capacity = N.Capacity(max_batch, num_ctas, max_qo_tokens, chunks_per_cta, max_gather_pages)
+        if schedule not in ("lpt", "equal"):
+            raise ValueError("schedule must be 'lpt' or 'equal'")
+        sched = N.BSP_SCHEDULE_LPT if schedule == "lpt" else N.BSP_SCHEDULE_EQUAL_SHARES
+        self.capacity = N.Capacity(max_batch, num_ctas, max_qo_tokens, chunks_per_cta, max_gather_pages, sched)
         ws_bytes = self.lib.bsp_workspace_size(ctypes.byref(self.problem), ctypes.byref(self.capacity))
         st_bytes = self.lib.bsp_host_staging_size(ctypes.byref(self.problem), ctypes.byref(self.capacity))
         if ws_bytes == 0 or st_bytes == 0:

@@ -48,6 +48,8 @@ bool compute_layout(const bsp_problem *p, const bsp_capacity *c, Layout *L) {
         return fail(BSP_ERR_INVALID_ARG, "capacity needs max_batch >= 0, num_ctas >= 1, max_qo_tokens >= 0"), false;
     if (c->chunks_per_cta < 0 || c->chunks_per_cta > 64)
         return fail(BSP_ERR_INVALID_ARG, "capacity.chunks_per_cta must be in [0, 64]"), false;
+    if (c->schedule != BSP_SCHEDULE_LPT && c->schedule != BSP_SCHEDULE_EQUAL_SHARES)
+        return fail(BSP_ERR_INVALID_ARG, "capacity.schedule must be BSP_SCHEDULE_LPT or BSP_SCHEDULE_EQUAL_SHARES"), false;
     if (c->max_gather_pages < 0 || (c->max_gather_pages > 0 && p->mode != BSP_MODE_PREFILL))
         return fail(BSP_ERR_INVALID_ARG, "capacity.max_gather_pages must be >= 0, and 0 in decode mode"), false;
     if ((int64_t)c->max_gather_pages * p->page_size > INT32_MAX)
@@ -180,10 +182,12 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
     Lc = (Lc + P.page_size - 1) / P.page_size * P.page_size;
     Lc = std::min<int64_t>(Lc, (int64_t)INT32_MAX / 2 / P.page_size * P.page_size);
 
-    // ---- 4: chunks of each tile's visible range, slots, reduction map ------
-    std::vector<Chunk> chunks;
-    std::vector<bsp_merge_entry> merges;
-    int32_t next_slot = 0;
+    // ---- 4: each output tile's visible range [lo, vis) -----------------------
+    struct TileRange {
+        int32_t b, tile, head, p0, p1;
+        int64_t lo, vis;
+    };
+    std::vector<TileRange> tiles;
     for (int b = 0; b < batch; ++b) {
         const int64_t qo_len = qo[b + 1] - qo[b];
         const int64_t kv_len = kv_len_of(kv_indptr_h, last_page_len_h, P.page_size, b);
@@ -200,58 +204,129 @@ extern "C" int bsp_plan(const bsp_problem *problem, const bsp_capacity *capacity
                 lo = lo / P.page_size * P.page_size;
                 if (lo >= vis) lo = vis = 0;  // nothing visible: one empty chunk
             }
-            const int64_t n = vis == lo ? 1 : (vis - lo + Lc - 1) / Lc;
-            for (int h = 0; h < H; ++h) {
-                if (n > 1) {
-                    bsp_merge_entry m{};
-                    m.b = b; m.tile = (int32_t)t; m.kv_head = h;
-                    m.slot_begin = next_slot; m.n_slots = (int32_t)n;
-                    m.q_tok0 = (int32_t)(qo[b] + p0); m.n_pos = (int32_t)(p1 - p0);
-                    merges.push_back(m);
-                }
-                for (int64_t i = 0; i < n; ++i) {
-                    Chunk ch;
-                    ch.b = b; ch.tile = (int32_t)t; ch.head = h;
-                    ch.start = (int32_t)std::min<int64_t>(lo + i * Lc, vis);
-                    ch.end = (int32_t)std::min<int64_t>(lo + (i + 1) * Lc, vis);
-                    ch.n_pos = (int32_t)(p1 - p0);
-                    ch.slot = n > 1 ? next_slot + (int32_t)i : -1;
-                    ch.merge = n > 1 ? (int32_t)merges.size() - 1 : -1;
-                    chunks.push_back(ch);
-                }
-                if (n > 1) next_slot += (int32_t)n;
-            }
+            for (int h = 0; h < H; ++h) tiles.push_back({b, (int32_t)t, h, (int32_t)p0, (int32_t)p1, lo, vis});
         }
     }
-    if ((int64_t)chunks.size() > lay.cap_items) return fail(BSP_ERR_CAPACITY, "work items exceed capacity");
-    if ((int64_t)merges.size() > lay.cap_merges) return fail(BSP_ERR_CAPACITY, "reduction map exceeds capacity");
-    if (next_slot > lay.cap_partials) return fail(BSP_ERR_CAPACITY, "partial states exceed capacity");
+    if ((int64_t)tiles.size() > lay.cap_items) return fail(BSP_ERR_CAPACITY, "work items exceed capacity");
 
-    // ---- 5: longest first; ties by the stable id (b, tile, kv_head, start) --
-    std::vector<int32_t> order(chunks.size());
-    for (size_t i = 0; i < order.size(); ++i) order[i] = (int32_t)i;
-    std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
-        const Chunk &a = chunks[x], &c = chunks[y];
-        const int32_t la = a.end - a.start, lc = c.end - c.start;
-        if (la != lc) return la > lc;
-        if (a.b != c.b) return a.b < c.b;
-        if (a.tile != c.tile) return a.tile < c.tile;
-        if (a.head != c.head) return a.head < c.head;
-        return a.start < c.start;
-    });
-
-    // ---- 6: LPT onto a min-heap of (cost, cta) ------------------------------
-    using Entry = std::pair<int64_t, int32_t>;
-    std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> heap;
-    for (int32_t c = 0; c < C; ++c) heap.push({0, c});
+    std::vector<Chunk> chunks;
+    std::vector<bsp_merge_entry> merges;
     std::vector<std::vector<int32_t>> queue(C);
-    for (int32_t idx : order) {
-        Entry e = heap.top();
-        heap.pop();
-        const Chunk &ch = chunks[idx];
-        queue[e.second].push_back(idx);
-        e.first += alpha * ch.n_pos + beta * (int64_t)(ch.end - ch.start);
-        heap.push(e);
+    int32_t next_slot = 0;
+    auto add_merge = [&](const TileRange &tr, int64_t n) {
+        bsp_merge_entry m{};
+        m.b = tr.b; m.tile = tr.tile; m.kv_head = tr.head;
+        m.slot_begin = next_slot; m.n_slots = (int32_t)n;
+        m.q_tok0 = (int32_t)(qo[tr.b] + tr.p0); m.n_pos = tr.p1 - tr.p0;
+        merges.push_back(m);
+    };
+    auto add_chunk = [&](const TileRange &tr, int64_t start, int64_t end, int64_t i, int64_t n) {
+        Chunk ch;
+        ch.b = tr.b; ch.tile = tr.tile; ch.head = tr.head;
+        ch.start = (int32_t)start; ch.end = (int32_t)end;
+        ch.n_pos = tr.p1 - tr.p0;
+        ch.slot = n > 1 ? next_slot + (int32_t)i : -1;
+        ch.merge = n > 1 ? (int32_t)merges.size() - 1 : -1;
+        chunks.push_back(ch);
+        return (int32_t)chunks.size() - 1;
+    };
+    auto check_bounds = [&]() -> bool {
+        if ((int64_t)chunks.size() > lay.cap_items) return fail(BSP_ERR_CAPACITY, "work items exceed capacity"), false;
+        if ((int64_t)merges.size() > lay.cap_merges)
+            return fail(BSP_ERR_CAPACITY, "reduction map exceeds capacity"), false;
+        if (next_slot > lay.cap_partials) return fail(BSP_ERR_CAPACITY, "partial states exceed capacity"), false;
+        return true;
+    };
+
+    if (capacity->schedule == BSP_SCHEDULE_EQUAL_SHARES) {
+        // ---- equal shares (not on the pages): the visible ranges end to end in
+        // (b, tile, kv_head) order, CTA c takes [floor(c V / C), floor((c+1) V / C)),
+        // a cut inside a tile moved down to a page boundary; each tile's pieces
+        // between cuts are its chunks, queued in the order of the concatenation.
+        std::vector<int64_t> start(tiles.size());
+        int64_t V = 0;
+        for (size_t i = 0; i < tiles.size(); ++i) {
+            start[i] = V;
+            V += tiles[i].vis - tiles[i].lo;
+        }
+        std::vector<int64_t> cut(C + 1);
+        size_t ti = 0;
+        for (int c = 0; c <= C; ++c) {
+            int64_t x = V * c / C;
+            if (c > 0 && c < C) {
+                while (ti < tiles.size() && start[ti] + (tiles[ti].vis - tiles[ti].lo) <= x) ++ti;
+                if (ti < tiles.size() && start[ti] < x) {  // strictly inside tile ti
+                    const int64_t key = tiles[ti].lo + (x - start[ti]);
+                    x = start[ti] + (key / P.page_size * P.page_size - tiles[ti].lo);
+                }
+            }
+            cut[c] = x;
+        }
+        int64_t longest = 1;
+        int c = 0;
+        for (size_t i = 0; i < tiles.size(); ++i) {
+            const TileRange &tr = tiles[i];
+            const int64_t P0 = start[i], n = tr.vis - tr.lo;
+            if (n == 0) {
+                int owner = c;
+                while (owner < C - 1 && cut[owner + 1] <= P0) ++owner;
+                queue[owner].push_back(add_chunk(tr, 0, 0, 0, 1));
+                continue;
+            }
+            // pieces: the shares [cut[c], cut[c+1]) that overlap [P0, P0 + n)
+            while (cut[c + 1] <= P0) ++c;
+            int64_t pieces = 0;
+            for (int cc = c; cc < C && cut[cc] < P0 + n; ++cc)
+                if (std::max(P0, cut[cc]) < std::min(P0 + n, cut[cc + 1])) ++pieces;
+            if (pieces > 1) add_merge(tr, pieces);
+            int64_t k = 0;
+            for (int cc = c; cc < C && cut[cc] < P0 + n; ++cc) {
+                const int64_t a = std::max(P0, cut[cc]), z = std::min(P0 + n, cut[cc + 1]);
+                if (a >= z) continue;
+                queue[cc].push_back(add_chunk(tr, tr.lo + a - P0, tr.lo + z - P0, k++, pieces));
+                longest = std::max(longest, z - a);
+            }
+            if (pieces > 1) next_slot += (int32_t)pieces;
+        }
+        Lc = longest;
+        if (!check_bounds()) return last_code();
+    } else {
+        // ---- 4 (cont.): chunks of at most L tokens, slots, reduction map -----
+        for (const TileRange &tr : tiles) {
+            const int64_t n = tr.vis == tr.lo ? 1 : (tr.vis - tr.lo + Lc - 1) / Lc;
+            if (n > 1) add_merge(tr, n);
+            for (int64_t i = 0; i < n; ++i)
+                add_chunk(tr, std::min<int64_t>(tr.lo + i * Lc, tr.vis), std::min<int64_t>(tr.lo + (i + 1) * Lc, tr.vis),
+                          i, n);
+            if (n > 1) next_slot += (int32_t)n;
+        }
+        if (!check_bounds()) return last_code();
+
+        // ---- 5: longest first; ties by the stable id (b, tile, kv_head, start) --
+        std::vector<int32_t> order(chunks.size());
+        for (size_t i = 0; i < order.size(); ++i) order[i] = (int32_t)i;
+        std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+            const Chunk &a = chunks[x], &c = chunks[y];
+            const int32_t la = a.end - a.start, lc = c.end - c.start;
+            if (la != lc) return la > lc;
+            if (a.b != c.b) return a.b < c.b;
+            if (a.tile != c.tile) return a.tile < c.tile;
+            if (a.head != c.head) return a.head < c.head;
+            return a.start < c.start;
+        });
+
+        // ---- 6: LPT onto a min-heap of (cost, cta) ------------------------------
+        using Entry = std::pair<int64_t, int32_t>;
+        std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> heap;
+        for (int32_t c = 0; c < C; ++c) heap.push({0, c});
+        for (int32_t idx : order) {
+            Entry e = heap.top();
+            heap.pop();
+            const Chunk &ch = chunks[idx];
+            queue[e.second].push_back(idx);
+            e.first += alpha * ch.n_pos + beta * (int64_t)(ch.end - ch.start);
+            heap.push(e);
+        }
     }
 
     // ---- write the staging image ---------------------------------------------

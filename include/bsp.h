@@ -80,6 +80,10 @@ typedef struct CUstream_st *bsp_stream_t; /* same type as cudaStream_t */
 #define BSP_DTYPE_BF16 0
 #define BSP_DTYPE_F32  1
 
+/* Work schedules of the plan (bsp_capacity.schedule). */
+#define BSP_SCHEDULE_LPT          0 /* the pages' plan: chunks of L tokens, longest first onto the least-loaded CTA */
+#define BSP_SCHEDULE_EQUAL_SHARES 1 /* not on the pages: equal contiguous shares of the concatenated KV ranges */
+
 #define BSP_MODE_DECODE  0 /* query tile = the g fused heads of one position */
 #define BSP_MODE_PREFILL 1 /* query tile = 256 packed rows (two MMA subtiles) */
 
@@ -142,6 +146,21 @@ typedef struct bsp_capacity {
                                pays when each KV token is read by several
                                query tiles (long prefills); larger tables run
                                the cp.async gather as without a region      */
+    int32_t schedule;       /* BSP_SCHEDULE_LPT (0, the pages' plan) or
+                               BSP_SCHEDULE_EQUAL_SHARES (1; not on the pages):
+                               the output tiles' visible KV ranges are laid end
+                               to end in (request, tile, kv head) order and CTA
+                               c takes the share [floor(c V / C),
+                               floor((c + 1) V / C)) of the V tokens, a cut
+                               inside a tile moved down to a page boundary. A
+                               tile's pieces between cuts are its chunks (its
+                               partial slots in order, as for LPT); an empty
+                               tile's one chunk goes to the first CTA whose share
+                               ends after its position. Every CTA gets the same
+                               KV (to within a page) in at most a few items:
+                               for batches of few, equal tiles, where LPT over
+                               whole tiles leaves CTAs idle. chunks_per_cta is
+                               ignored; the bounds hold with s = 1           */
 } bsp_capacity;
 
 /* One work item of the plan (64 bytes, device and staging image). */
@@ -180,7 +199,8 @@ typedef struct bsp_plan_info {
     int32_t batch;
     int32_t tile_rows;      /* T_q packed rows per query tile                     */
     int32_t group;          /* g                                                  */
-    int32_t chunk_len;      /* L: maximum KV tokens per chunk                     */
+    int32_t chunk_len;      /* L: maximum KV tokens per chunk (equal shares: the
+                               longest chunk of the plan)                         */
     int64_t total_work;     /* W                                                  */
     int64_t alpha, beta;    /* cost = alpha * positions + beta * chunk tokens     */
     int32_t num_items;

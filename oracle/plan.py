@@ -42,9 +42,24 @@ Attention Engine, §VIII.2 and §VIII.5):
    output; one with several chunks gets consecutive partial slots in ascending
    chunk_start order, numbered over output tiles in (b, tile, kv_head) order,
    and its final state is the left-to-right merge of those slots.
+
+Equal shares (schedule="equal"; not on the pages, this build's extension for
+batches of few, equal tiles, where LPT over whole tiles leaves CTAs idle):
+steps 1-2 as above; then the output tiles' visible ranges [lo, v) are laid end
+to end in (b, tile, kv_head) order (tile i starts at P_i, n_i = v_i - lo_i
+tokens, V = sum n_i), and CTA c takes the share [x_c, x_{c+1}) with
+x_c = floor(c V / C). A cut that falls strictly inside a tile is moved down to
+the page boundary at or before it (key lo_i + x - P_i rounded down to a multiple
+of page_size), so that chunks start on pages. A tile's chunks are its non-empty
+pieces between consecutive cuts, each on the CTA whose share holds it, in
+order; a tile with nothing visible gets one empty chunk on the first CTA whose
+share ends after P_i (the last CTA if none). Queues hold their chunks in the
+order of the concatenation; the reduction map is step 7's. L is reported as
+the longest chunk.
 """
 from __future__ import annotations
 
+import bisect
 import heapq
 from dataclasses import dataclass, field
 
@@ -106,7 +121,7 @@ def visible_len(qo_len: int, kv_len: int, last_pos: int, causal: bool) -> int:
 
 def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
          num_ctas: int, page_size: int, causal: bool, alpha: int = 2, beta: int = 1,
-         window_left: int = -1, chunks_per_cta: int = 1) -> Plan:
+         window_left: int = -1, chunks_per_cta: int = 1, schedule: str = "lpt") -> Plan:
     if tile_rows % group != 0:
         raise ValueError("tile_rows must be a multiple of the group size")
     if num_ctas < 1 or page_size < 1:
@@ -128,6 +143,11 @@ def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
             for h in range(num_kv_heads):
                 tiles.append((b, t, h, p1 - p0, lo, vis))
                 W += kv_lens[b]
+
+    if schedule == "equal":
+        return equal_shares(tiles, W, num_ctas, page_size, alpha, beta, tile_rows)
+    if schedule != "lpt":
+        raise ValueError("schedule must be 'lpt' or 'equal'")
 
     # 3: chunk length; s = chunks_per_cta > 1 divides it further (s = 1 is the
     # pages' L = ceil(W / C))
@@ -166,6 +186,55 @@ def plan(qo_lens, kv_lens, num_kv_heads: int, group: int, tile_rows: int,
 
     return Plan(tile_rows=tile_rows, chunk_len=L, total_work=W, queues=queues,
                 outputs=outputs, num_partials=next_slot, cta_cost=cta_cost)
+
+
+def equal_shares(tiles, W: int, num_ctas: int, page_size: int, alpha: int, beta: int, tile_rows: int) -> Plan:
+    """The equal-share schedule (module docstring) over the output tiles
+    (b, tile, kv_head, l_q, lo, visible) of steps 1-2."""
+    starts, V = [], 0
+    for (_, _, _, _, lo, vis) in tiles:
+        starts.append(V)
+        V += vis - lo
+    cuts = [c * V // num_ctas for c in range(num_ctas + 1)]
+    for c in range(1, num_ctas):
+        i = bisect.bisect_right(starts, cuts[c]) - 1  # the last tile starting at or before the cut
+        while i >= 0 and tiles[i][5] == tiles[i][4]:  # (an empty tile has no inside)
+            i -= 1
+        if i >= 0:
+            lo, vis = tiles[i][4], tiles[i][5]
+            P, n = starts[i], vis - lo
+            if P < cuts[c] < P + n:
+                key = lo + cuts[c] - P
+                cuts[c] = P + (key // page_size * page_size - lo)
+    queues = [[] for _ in range(num_ctas)]
+    outputs = []
+    next_slot = 0
+    longest = 1
+    for i, (b, t, h, lq, lo, vis) in enumerate(tiles):
+        P, n = starts[i], vis - lo
+        first = bisect.bisect_right(cuts, P, lo=1) - 1  # first CTA whose share ends after P
+        if n == 0:
+            owner = min(first, num_ctas - 1)
+            queues[owner].append(Item(b, t, h, 0, 0, -1))
+            continue
+        pieces = []
+        for c in range(first, num_ctas):
+            a, z = max(P, cuts[c]), min(P + n, cuts[c + 1])
+            if cuts[c] >= P + n:
+                break
+            if a < z:
+                pieces.append((c, lo + a - P, lo + z - P))
+        if len(pieces) > 1:
+            outputs.append(Output(b, t, h, next_slot, len(pieces)))
+        for k, (c, s, e) in enumerate(pieces):
+            queues[c].append(Item(b, t, h, s, e, next_slot + k if len(pieces) > 1 else -1))
+            longest = max(longest, e - s)
+        if len(pieces) > 1:
+            next_slot += len(pieces)
+    lq_of = {(b, t): lq for (b, t, _, lq, _, _) in tiles}
+    cta_cost = [sum(alpha * lq_of[(it.b, it.tile)] + beta * (it.kv_end - it.kv_start) for it in q) for q in queues]
+    return Plan(tile_rows=tile_rows, chunk_len=longest, total_work=W, queues=queues, outputs=outputs,
+                num_partials=next_slot, cta_cost=cta_cost)
 
 
 def makespan_lower_bound(costs, num_ctas: int) -> float:

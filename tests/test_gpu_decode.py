@@ -83,6 +83,32 @@ def test_vector_sparse_permuted_equals_contiguous(bsp):
     compare(out_p, lse_p, O, L, "bf16", oracle_s=t)
 
 
+def test_vector_sparse_equal_shares(bsp):
+    """The page-size-1 decode with the equal-share schedule (every CTA 6898-6899
+    tokens in at most 3 items, most tiles split): permuted and contiguous layouts
+    bitwise equal, every output row against the oracle."""
+    perm, cont = workloads.vector_sparse_decode_bf16()
+    out_p, lse_p, pa = run_batch(bsp, perm, schedule="equal")
+    assert pa.info.num_merges > 0
+    out_c, lse_c, _ = run_batch(bsp, cont, schedule="equal")
+    assert torch.equal(out_p, out_c) and torch.equal(lse_p, lse_c)
+    (O, L), t = timed(oracle_full, perm)
+    compare(out_p, lse_p, O, L, "bf16", oracle_s=t)
+    assert pa.check_device_error() == 0
+
+
+@pytest.mark.parametrize("case", CASES[:8], ids=[f"equal{c[0]}" for c in CASES[:8]])
+def test_random_equal_share_decode(bsp, case):
+    """Random decode batches under the equal-share schedule (splits inside
+    requests at page boundaries, empty requests, several items per CTA)."""
+    seed, kv, hq, hk, D, ps, C = case
+    b = workloads.paged_batch(seed, np.ones(len(kv), int), kv, hq, hk, D, ps, "bf16", extra_pages=3)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, num_ctas=C, schedule="equal")
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
 @pytest.mark.parametrize("ps,D", [(16, 128), (8, 64), (64, 128)])
 def test_tma_gather_equals_cp_async_gather(bsp, ps, D):
     """Pages of 8 or more tokens are gathered by TMA page boxes when the pool

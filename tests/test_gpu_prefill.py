@@ -314,6 +314,18 @@ def test_gathered_prefill_variants_and_sink(bsp):
     assert pa.check_device_error() == 0
 
 
+def test_equal_share_prefill(bsp):
+    """Causal ragged prefill under the equal-share schedule (tiles split across
+    CTAs at page boundaries, merged by the reduce kernel); against the oracle."""
+    b = workloads.paged_batch(137, [300, 65, 1000, 1], [300, 65, 1000, 0], 32, 8, 128, 16, "bf16", causal=True,
+                              extra_pages=2)
+    O, L = oracle_full(b)
+    out, lse, pa = run_batch(bsp, b, mode="prefill", num_ctas=23, schedule="equal")
+    assert pa.info.num_merges > 0
+    compare(out, lse, O, L, "bf16")
+    assert pa.check_device_error() == 0
+
+
 def test_gather_reports_page_ids_out_of_range(bsp):
     """The gather checks every page id against the pool size: an id outside it
     gives a zero page and the status word 0x301 (no out-of-range read)."""

@@ -168,8 +168,64 @@ def pin_traffic_ratio(pl):
     assert pl.prefix_traffic_ratio(64, 8192, 0) == pytest.approx(64.0)
 
 
+def pin_equal_share_example(pl):
+    """Equal shares (this build's extension) on a case worked out by hand from
+    the definition: two 10-token decode requests, one kv head, 3 CTAs. V = 20,
+    cuts floor(20/3) = 6 and floor(40/3) = 13. Page size 1: CTA 0 takes [0, 6)
+    of request 0, CTA 1 its [6, 10) and [0, 3) of request 1, CTA 2 [3, 10);
+    both requests split in two (slots 0, 1 and 2, 3). Page size 4: cut 6 moves
+    down to key 4, cut 13 (key 3 of request 1) down to key 0, the start of
+    request 1: [0, 4) | [4, 10) | request 1 whole."""
+    p = pl.plan([1, 1], [10, 10], 1, 1, 1, 3, 1, False, schedule="equal")
+    got = [[(it.b, it.kv_start, it.kv_end, it.slot) for it in q] for q in p.queues]
+    assert got == [[(0, 0, 6, 0)], [(0, 6, 10, 1), (1, 0, 3, 2)], [(1, 3, 10, 3)]], got
+    assert [(o.b, o.slot_begin, o.n_slots) for o in p.outputs] == [(0, 0, 2), (1, 2, 2)]
+    p = pl.plan([1, 1], [10, 10], 1, 1, 1, 3, 4, False, schedule="equal")
+    got = [[(it.b, it.kv_start, it.kv_end, it.slot) for it in q] for q in p.queues]
+    assert got == [[(0, 0, 4, 0)], [(0, 4, 10, 1)], [(1, 0, 10, -1)]], got
+    assert p.chunk_len == 10 and p.num_partials == 2
+
+
+def pin_equal_share_balance(pl):
+    """Equal shares: every (request, kv head, visible position) exactly once; each
+    CTA's KV within a page of V / C (ceil(V / C) + page_size - 1 at most, floor(V / C)
+    - (page_size - 1) at least, for shares that do not end at a tile's end);
+    queues in the order of the concatenation; at most tiles + C - 1 chunks."""
+    for c in _cases():
+        p = pl.plan(c["qo"], c["kv"], c["hk"], c["g"], c["tile"], c["C"], c["ps"], c["causal"], schedule="equal")
+        order = []  # (b, tile, kv_head) in concatenation order with their visible lengths
+        for b in range(len(c["qo"])):
+            ntile = -(-c["qo"][b] * c["g"] // c["tile"])
+            for t in range(ntile):
+                per = c["tile"] // c["g"]
+                last_pos = min(c["qo"][b], (t + 1) * per) - 1
+                vis = c["kv"][b] if not c["causal"] else max(0, min(c["kv"][b], last_pos + c["kv"][b] - c["qo"][b] + 1))
+                for h in range(c["hk"]):
+                    order.append(((b, t, h), vis))
+        V = sum(v for _, v in order)
+        pos = {}
+        acc = 0
+        for key, v in order:
+            pos[key] = acc
+            acc += v
+        items = [it for q in p.queues for it in q]
+        assert len(items) <= len(order) + c["C"] - 1
+        cover = {}
+        for it in items:
+            cover.setdefault((it.b, it.tile, it.kv_head), []).extend(range(it.kv_start, it.kv_end))
+        assert set(cover) == {key for key, _ in order}  # every tile has a chunk, empty tiles one empty chunk
+        for key, v in order:
+            assert sorted(cover[key]) == list(range(v)), (c, key)
+        for ci, q in enumerate(p.queues):
+            load = sum(it.kv_end - it.kv_start for it in q)
+            assert load <= -(-V // c["C"]) + c["ps"] - 1, (c, ci, load)
+            starts = [pos[(it.b, it.tile, it.kv_head)] + it.kv_start for it in q if it.kv_end > it.kv_start]
+            assert starts == sorted(starts)
+
+
 ALL_PLAN_PINS = [pin_lpt_worked_example, pin_capacity_formula, pin_coverage, pin_chunk_len_and_bounds,
-                 pin_lpt_quality, pin_determinism, pin_empty_tiles, pin_chunks_per_cta, pin_traffic_ratio]
+                 pin_lpt_quality, pin_determinism, pin_empty_tiles, pin_chunks_per_cta, pin_traffic_ratio,
+                 pin_equal_share_example, pin_equal_share_balance]
 
 
 @pytest.mark.parametrize("pin", ALL_PLAN_PINS, ids=lambda f: f.__name__)
@@ -193,6 +249,12 @@ PLAN_MUTATIONS = [
     ("no_empty_chunk", "or [(0, 0)]", "or []"),
     ("slots_not_consecutive", "chunks.append((b, t, h, s, e, lq, next_slot + i))",
      "chunks.append((b, t, h, s, e, lq, next_slot + 2 * i))"),
+    ("equal_cuts_rounded_up", "cuts = [c * V // num_ctas for c in range(num_ctas + 1)]",
+     "cuts = [-(-c * V // num_ctas) for c in range(num_ctas + 1)]"),
+    ("equal_cuts_not_on_pages", "cuts[c] = P + (key // page_size * page_size - lo)", "cuts[c] = P + (key - lo)"),
+    ("equal_empty_tile_dropped", "queues[owner].append(Item(b, t, h, 0, 0, -1))", "pass"),
+    ("equal_slots_shared", "queues[c].append(Item(b, t, h, s, e, next_slot + k if len(pieces) > 1 else -1))",
+     "queues[c].append(Item(b, t, h, s, e, next_slot if len(pieces) > 1 else -1))"),
 ]
 
 

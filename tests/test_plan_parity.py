@@ -16,7 +16,7 @@ def bsp():
 
 
 def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alpha=2, beta=1, D=128,
-             max_batch=None, max_qo=None, window_left=-1, s=1):
+             max_batch=None, max_qo=None, window_left=-1, s=1, schedule="lpt"):
     qo_lens = np.asarray(qo_lens, np.int64)
     kv_lens = np.asarray(kv_lens, np.int64)
     B = len(kv_lens)
@@ -29,13 +29,14 @@ def run_both(bsp, mode, qo_lens, kv_lens, page_size, H_qo, H_kv, causal, C, alph
     g = H_qo // H_kv
     prob = bsp.make_problem(mode, H_qo, H_kv, D, page_size, causal, __import__("torch").bfloat16,
                             window_left=window_left)
-    cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]), s)
+    sched = bsp._native.BSP_SCHEDULE_EQUAL_SHARES if schedule == "equal" else bsp._native.BSP_SCHEDULE_LPT
+    cap = bsp.Capacity(max_batch or B, C, max_qo or int(qo_indptr[-1]), s, 0, sched)
     info, queue, items, merges = bsp.plan_host(prob, cap, kv_indptr, last,
                                                None if mode == bsp.BSP_MODE_DECODE and np.all(qo_lens == 1) else qo_indptr,
                                                alpha, beta)
     tile = g if mode == bsp.BSP_MODE_DECODE else 256
     ref = oplan.plan(qo_lens.tolist(), kv_lens.tolist(), H_kv, g, tile, C, page_size, causal, alpha, beta,
-                     window_left=window_left, chunks_per_cta=s)
+                     window_left=window_left, chunks_per_cta=s, schedule=schedule)
     return info, queue, items, merges, ref, qo_indptr, kv_indptr
 
 
@@ -129,13 +130,13 @@ def test_vector_sparse_decode_balance_with_chunks_per_cta(bsp):
 
 
 def test_benchmark_workload_lengths(bsp):
-    b2 = workloads.batched_decode_bf16()
-    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, b2.qo_lens, b2.kv_lens, 16, 32, 8, False, 304))
-    b4 = workloads.ragged_causal_prefill_bf16()
-    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, b4.qo_lens, b4.kv_lens, 16, 32, 8, True, 152))
-    sp = workloads.shared_prefix_decode_bf16()
-    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, sp.prefix.qo_lens, sp.prefix.kv_lens, 16, 32, 8, False, 152))
-    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, sp.suffix.qo_lens, sp.suffix.kv_lens, 16, 32, 8, False, 304))
+    _, kv2 = workloads.batched_decode_lengths()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(64, int), kv2, 16, 32, 8, False, 304))
+    _, l4 = workloads.ragged_causal_prefill_lengths()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, l4, l4, 16, 32, 8, True, 152))
+    _, suf = workloads.shared_prefix_suffix_lengths()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_PREFILL, [64], [8192], 16, 32, 8, False, 152))
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(64, int), suf, 16, 32, 8, False, 304))
 
 
 def test_capacity_and_metadata_errors(bsp):
@@ -205,3 +206,48 @@ def test_window_plan_parity_and_coverage(bsp, case):
             if vis_hi > vis_lo:
                 assert lo <= vis_lo and vis_hi <= hi, (b, t, p, lo, hi, vis_lo, vis_hi)
                 assert lo % ps == 0
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_equal_share_plans(bsp, seed):
+    """The equal-share schedule: C++ and oracle planners bit-exact on random
+    decode and prefill batches (windows and empty requests included), within
+    the s = 1 capacity bounds."""
+    rng = np.random.default_rng(7000 + seed)
+    B = int(rng.integers(1, 40))
+    H_kv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    ps = int(rng.choice([1, 3, 16, 64]))
+    C = int(rng.integers(1, 400))
+    kv = rng.integers(0, 5000, size=B)
+    kv[rng.random(B) < 0.1] = 0
+    w = int(rng.choice([-1, 300])) if seed % 3 == 0 else -1
+    if seed % 2 == 0:
+        out = run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(B, int), kv, ps, H_kv * g, H_kv, False, C, alpha=64,
+                       window_left=w, schedule="equal")
+    else:
+        causal = bool(seed % 3)
+        qo = np.maximum(1, np.minimum(np.maximum(kv, 1), rng.integers(1, 700, size=B))) if causal else rng.integers(1, 700, size=B)
+        out = run_both(bsp, bsp.BSP_MODE_PREFILL, qo, kv, ps, H_kv * g, H_kv, causal, C, window_left=w,
+                       schedule="equal")
+    assert_same(*out)
+    info = out[0]
+    assert info.num_items <= info.cap_items and info.num_partials <= info.cap_partials
+
+
+def test_equal_share_benchmark_workloads(bsp):
+    """The page-size-1 decode (32 x 4096 tokens, 8 kv heads) on 152 CTAs: every CTA
+    gets 6898 or 6899 tokens in at most 3 items; and the other decode workloads."""
+    out = run_both(bsp, bsp.BSP_MODE_DECODE, [1] * 32, [4096] * 32, 1, 64, 8, False, 152, alpha=64,
+                   schedule="equal")
+    assert_same(*out)
+    ref = out[4]
+    loads = [sum(it.kv_end - it.kv_start for it in q) for q in ref.queues]
+    assert set(loads) <= {6898, 6899}
+    assert max(len(q) for q in ref.queues) <= 3
+    _, kv2 = workloads.batched_decode_lengths()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(64, int), kv2, 16, 32, 8, False, 152, alpha=64,
+                          schedule="equal"))
+    _, suf = workloads.shared_prefix_suffix_lengths()
+    assert_same(*run_both(bsp, bsp.BSP_MODE_DECODE, np.ones(64, int), suf, 16, 32, 8, False, 120, alpha=64,
+                          schedule="equal"))

@@ -157,11 +157,16 @@ def tiny_decode_f32() -> PagedBatch:
                       v_pages=v)
 
 
+def batched_decode_lengths(batch: int = 64, seed: int = 2):
+    """(generator after the draw, KV lengths) of the batched decode: U{512..8192}."""
+    rng = np.random.default_rng(seed)
+    return rng, rng.integers(512, 8192, size=batch, endpoint=True)
+
+
 def batched_decode_bf16(batch: int = 64, seed: int = 2) -> PagedBatch:
     """Llama-3-8B layer shape: batch 64, KV ~ U{512..8192}, page 16, a pool sized to
     the total and permuted, 32 qo / 8 kv heads, head_dim 128, bf16."""
-    rng = np.random.default_rng(seed)
-    kv = rng.integers(512, 8192, size=batch, endpoint=True)
+    rng, kv = batched_decode_lengths(batch, seed)
     b = paged_batch(seed, np.ones(batch, np.int64), kv, 32, 8, 128, 16, "bf16", rng=rng,
                     name="batched_decode_bf16")
     return b
@@ -260,11 +265,16 @@ def vector_sparse_prefill_bf16(length: int = 32768, seed: int = 6, num_qo_heads:
     return permuted, contiguous
 
 
+def ragged_causal_prefill_lengths(batch: int = 16, seed: int = 4):
+    """(generator after the draw, lengths) of the ragged causal prefill: qo = kv ~ U{128..2048}."""
+    rng = np.random.default_rng(seed)
+    return rng, rng.integers(128, 2048, size=batch, endpoint=True)
+
+
 def ragged_causal_prefill_bf16(batch: int = 16, seed: int = 4) -> PagedBatch:
     """batch 16, qo = kv ~ U{128..2048}, ragged Q, page 16 permuted, 32 qo / 8 kv
     heads, head_dim 128, bf16, causal (bottom-right)."""
-    rng = np.random.default_rng(seed)
-    lens = rng.integers(128, 2048, size=batch, endpoint=True)
+    rng, lens = ragged_causal_prefill_lengths(batch, seed)
     return paged_batch(seed, lens, lens, 32, 8, 128, 16, "bf16", causal=True, rng=rng,
                        name="ragged_causal_prefill_bf16")
 
@@ -279,6 +289,16 @@ class SharedPrefixBatch:
     suffix_lens: np.ndarray
 
 
+def shared_prefix_suffix_lengths(batch: int = 64, outlier: int = 32768, suffix_lo: int = 64, suffix_hi: int = 1024,
+                                 seed: int = 5):
+    """(generator after the draw, suffix lengths) of the shared-prefix decode:
+    U{suffix_lo..suffix_hi}, the last one the outlier."""
+    rng = np.random.default_rng(seed)
+    suffix = rng.integers(suffix_lo, suffix_hi, size=batch, endpoint=True)
+    suffix[-1] = outlier
+    return rng, suffix
+
+
 def shared_prefix_decode_bf16(batch: int = 64, prefix_len: int = 8192, outlier: int = 32768,
                               suffix_lo: int = 64, suffix_hi: int = 1024, seed: int = 5,
                               num_qo_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
@@ -286,9 +306,7 @@ def shared_prefix_decode_bf16(batch: int = 64, prefix_len: int = 8192, outlier: 
     """64 decode requests sharing an 8192-token prefix (512 pages of 16); suffixes
     ~ U{64..1024} for the first 63 requests and 32768 tokens for the last one
     (the skewed outlier); 32 qo / 8 kv heads, head_dim 128, bf16."""
-    rng = np.random.default_rng(seed)
-    suffix = rng.integers(suffix_lo, suffix_hi, size=batch, endpoint=True)
-    suffix[-1] = outlier
+    rng, suffix = shared_prefix_suffix_lengths(batch, outlier, suffix_lo, suffix_hi, seed)
     assert prefix_len % page_size == 0
     n_prefix_pages = prefix_len // page_size
     s_pages, s_last = _pages_for(suffix, page_size)
