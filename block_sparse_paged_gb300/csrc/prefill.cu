@@ -504,10 +504,13 @@ __global__ void __launch_bounds__(kTma ? kThreads : kThreadsGather, 1)
                     // visible columns of this row: [c_lo, c_hi)
                     const int c_hi = min(valid, lim == INT_MAX ? kKvTile : max(0, min(kKvTile, lim - tok0 + 1)));
                     const int c_lo = kVar && lo != INT_MIN ? max(0, lo - tok0) : 0;
+                    // a late row's window can start past this KV tile (a 256-row tile
+                    // spans 128+ positions when g <= 2): nothing visible then
+                    const int c_w = max(0, c_hi - c_lo);
                     if (kVar) {
 #pragma unroll
                         for (int c = 0; c < kKvTile; ++c)
-                            sv[c] = (unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) ? sv[c] : -INFINITY;
+                            sv[c] = (unsigned)(c - c_lo) < (unsigned)c_w ? sv[c] : -INFINITY;
                     } else {
 #pragma unroll
                         for (int c = 0; c < kKvTile; ++c) sv[c] = c < c_hi ? sv[c] : -INFINITY;

@@ -46,6 +46,10 @@ PREFILL = [
     (96, [300, 65, 1000], [300, 65, 1000], 32, 8, 16, True, -1, 1.5, 13),
     (97, [200, 90], [700, 90], 16, 4, 1, True, 77, 2.5, 7),      # page size 1, qo < kv, both
     (98, [128, 300], [128, 500], 32, 8, 32, False, 100, 0.0, 9),  # non-causal window
+    # a tile spans 256 (g = 1) or 128 (g = 2) positions: late rows' windows start
+    # past a whole 128-key tile that earlier rows of the same tile still see
+    (99, [400, 70], [400, 900], 16, 16, 16, True, 40, 0.0, 11),
+    (100, [300, 129], [300, 129], 16, 8, 16, True, 64, 1.0, 5),
 ]
 
 
