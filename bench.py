@@ -424,12 +424,15 @@ def run_e2e(bsp, batch, pa, K, W, dev, nbytes, world):
             "note": "KV pool, Q and page table copied from pinned host memory every step"}
 
 
-def oracle_timed(batch, tok, head, seconds: float, threads: int = 0):
+def oracle_timed(batch, tok, head, seconds: float, threads: int = 0, k32=None, v32=None):
     """(repetitions, seconds) of the oracle, as it stands, over the selected
-    (token, head) rows, repeated for about `seconds` (at least once)."""
+    (token, head) rows, repeated for about `seconds` (at least once). k32 / v32:
+    the pools' values as float32 (default: the batch's own pools)."""
     import oracle
-    k32 = batch.k_pages.float().numpy()
-    v32 = batch.v_pages.float().numpy()
+    if k32 is None:
+        k32 = batch.k_pages.float().numpy()
+    if v32 is None:
+        v32 = batch.v_pages.float().numpy()
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.attention_rows_of(batch, tok, head, num_threads=threads, k_f32=k32, v_f32=v32)
@@ -495,6 +498,17 @@ def workloads_sub(batch, n_req):
                             last_page_len=batch.last_page_len[:n_req])
 
 
+def cpu_baseline_decode(batch, nbytes: float, seconds: float, what: str, k32=None, v32=None):
+    """The oracle on all host cores over every output row of `batch`, repeated
+    for about `seconds`; `nbytes` (the line's algorithmic bytes per run) per
+    repetition gives the line's own unit."""
+    import oracle
+    tok, head = all_rows(batch)
+    reps, el = oracle_timed(batch, tok, head, seconds, k32=k32, v32=v32)
+    return {"value": round(nbytes * reps / el / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads_available(),
+            "kind": "oracle", "sample": f"{what}: every output row, {reps} repetitions in {el:.1f} s, fp64"}
+
+
 def cpu_baseline_prefill(batch, stride: int, seed: int, seconds: float):
     """The oracle on all host cores over a seeded 1/stride sample of the rows
     (every request and head), repeated for about `seconds`: GFLOP/s over the
@@ -514,7 +528,7 @@ def secondary(bsp, dev, args, pk):
     steps = max(5, min(args.steps, 50))
     warm = max(3, args.warmup)
     cpu = 0.0 if args.no_cpu_baseline else args.cpu_seconds / 2
-    res["vector_sparse_decode"] = vector_sparse_decode(bsp, dev, steps, warm, pk, args.num_ctas)
+    res["vector_sparse_decode"] = vector_sparse_decode(bsp, dev, steps, warm, pk, args.num_ctas, cpu)
     torch.cuda.empty_cache()
     res["ragged_causal_prefill"] = ragged_prefill(bsp, dev, steps, warm, pk, cpu)
     torch.cuda.empty_cache()
@@ -522,8 +536,8 @@ def secondary(bsp, dev, args, pk):
     torch.cuda.empty_cache()
     res["bsr_prefill"] = bsr_prefill(bsp, dev, steps, warm, pk, cpu)
     torch.cuda.empty_cache()
-    res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk)
-    res["fp8_kv_decode"] = fp8_decode(bsp, dev, steps, warm, pk)
+    res["shared_prefix_decode"] = shared_prefix(bsp, dev, steps, warm, pk, cpu)
+    res["fp8_kv_decode"] = fp8_decode(bsp, dev, steps, warm, pk, cpu)
     res["tiny_decode_f32"] = tiny_decode_f32(bsp, dev, steps, warm, pk)
     return res
 
@@ -552,6 +566,9 @@ def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0
         del pa, q, k, v, out, lse
         torch.cuda.empty_cache()
     r["permuted_over_contiguous"] = round(r["permuted"]["GB/s"] / r["contiguous"]["GB/s"], 4)
+    if cpu_seconds > 0:
+        r["cpu_baseline"] = cpu_baseline_decode(perm, decode_bytes(perm), cpu_seconds,
+                                                "the permuted page-size-1 workload (32 requests x 64 heads)")
     r["workload"] = ("32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16; "
                      "equal-share plan (permuted_lpt: the pages' LPT plan); one launch per run, 10 per graph replay")
     r["roofline"] = {"bound": "hbm", "kernel": "decode_bf16_kernel<128, cp.async gather>",
@@ -668,7 +685,7 @@ def graph_time(run, st, steps, warm, reps=10):
     return ms
 
 
-def fp8_decode(bsp, dev, steps, warm, pk):
+def fp8_decode(bsp, dev, steps, warm, pk, cpu_seconds=0.0):
     """The batched decode workload with e4m3 K / V pools (one scale each):
     algorithmic bytes as for bf16 but one byte per K / V element."""
     import workloads
@@ -693,7 +710,15 @@ def fp8_decode(bsp, dev, steps, warm, pk):
     gbs = nbytes / (ms * 1e-3) / 1e9
     del pa, q, k, v
     torch.cuda.empty_cache()
-    return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
+    cpu = {}
+    if cpu_seconds > 0:
+        import oracle.fp8
+        # the oracle over the values the codes stand for (k_scale * value(code))
+        k32 = oracle.fp8.dequantize(f8.k8.numpy(), f8.k_scale).astype(np.float32)
+        v32 = oracle.fp8.dequantize(f8.v8.numpy(), f8.v_scale).astype(np.float32)
+        cpu["cpu_baseline"] = cpu_baseline_decode(b, nbytes, cpu_seconds, "the e4m3 batched decode (64 requests x "
+                                                  "32 heads, codes decoded once outside the timing)", k32=k32, v32=v32)
+    return {**cpu, "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
             "bytes": nbytes, "tokens_per_s": round(b.batch / (ms * 1e-3), 1),
             "workload": "batched decode (64 requests, KV ~ U{512..8192}, page 16 permuted, 32/8 heads, D 128), "
                         "K / V e4m3 with one scale per pool, q / o bf16; one launch per step, 10 per graph replay",
@@ -770,7 +795,7 @@ def shared_prefix_split(bsp, dev, prefix_tiles: int = 8):
     return min(c, sms - 8), sms
 
 
-def shared_prefix(bsp, dev, steps, warm, pk):
+def shared_prefix(bsp, dev, steps, warm, pk, cpu_seconds=0.0):
     """Composable decode: prefix view on the prefill kernel (all 64 queries as one
     row block over the shared pages) and suffix view on the decode kernel, run
     concurrently on two streams over disjoint SM counts (their plans are made
@@ -832,7 +857,13 @@ def shared_prefix(bsp, dev, steps, warm, pk):
     n, P, S = sp.full.batch, sp.prefix_len, float(sp.suffix_lens.mean())
     ratio = n * (P + S) / (P + n * S)
     del graph
-    return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
+    cpu = {}
+    if cpu_seconds > 0:
+        # the oracle computes each request over its whole KV (prefix and suffix),
+        # timed against the same prefix-once bytes as the line
+        cpu["cpu_baseline"] = cpu_baseline_decode(sp.full, nbytes, cpu_seconds,
+                                                  "each of the 64 requests over its prefix and suffix")
+    return {**cpu, "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "ms": round(ms, 4),
             "algorithmic_bytes": nbytes, "launches_per_step": 4, "ctas_prefix_view": c_pre,
             "ctas_suffix_view": sms - c_pre, "eq15_traffic_ratio": round(ratio, 3),
             "workload": "64 decode requests sharing an 8192-token prefix, suffixes U{64..1024} and one 32768 "
