@@ -544,13 +544,13 @@ def secondary(bsp, dev, args, pk):
 
 def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0.0):
     """Page size 1 (every token slot permuted) vs the same KV contiguous: GB/s
-    of each and their ratio, under the equal-share schedule (256 equal tiles on
-    152 CTAs: LPT over whole tiles leaves 48 CTAs with half the work), and the
-    permuted layout under the pages' LPT plan for comparison."""
+    of each and their ratio under the pages' LPT plan, and the permuted layout
+    under the equal-share schedule for comparison (it evens out the 256 equal
+    tiles on 152 CTAs, but adds split outputs and their fold)."""
     import workloads
     perm, cont = workloads.vector_sparse_decode_bf16()
     r = {}
-    for tag, b, sched in (("permuted", perm, "equal"), ("contiguous", cont, "equal"), ("permuted_lpt", perm, "lpt")):
+    for tag, b, sched in (("permuted", perm, "lpt"), ("contiguous", cont, "lpt"), ("permuted_equal", perm, "equal")):
         C = num_ctas or bsp.default_num_ctas(bsp.BSP_MODE_DECODE, dev.index)
         pa = bsp.PagedAttention("decode", b.num_qo_heads, b.num_kv_heads, b.head_dim, 1, False, torch.bfloat16,
                                 max_batch=b.batch, num_ctas=C, device=dev, schedule=sched)
@@ -570,7 +570,7 @@ def vector_sparse_decode(bsp, dev, steps, warm, pk, num_ctas=None, cpu_seconds=0
         r["cpu_baseline"] = cpu_baseline_decode(perm, decode_bytes(perm), cpu_seconds,
                                                 "the permuted page-size-1 workload (32 requests x 64 heads)")
     r["workload"] = ("32 requests x 4096 tokens, page size 1 (131072 slots permuted), 64/8 heads, D 128, bf16; "
-                     "equal-share plan (permuted_lpt: the pages' LPT plan); one launch per run, 10 per graph replay")
+                     "the pages' LPT plan (permuted_equal: the equal-share plan); one launch per run, 10 per graph replay")
     r["roofline"] = {"bound": "hbm", "kernel": "decode_bf16_kernel<128, cp.async gather>",
                      "achieved": r["permuted"]["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": r["permuted"]["frac_of_hbm"], "peak_source": "measured (STREAM-style copy)",

@@ -7,12 +7,15 @@
 // each loaded KV tile (head-group fusion, technical review eq 3; overview ⑦).
 //
 // bf16 kernel (one persistent CTA per SM, running its plan queue(s)):
-//   - loaders (warp 4: K, warp 5: V) fill a ring of stages through the page
-//     table (sparse gather, dense compute: overview ⑥, walkthrough §IV.2 and
-//     §V.4). Pages of 8 or more tokens: one TMA tensor copy per page box
-//     (up to 64 rows of one kv head, 128-byte swizzle), page ids read 32 boxes
-//     at a time one batch ahead. Smaller pages: 16-byte cp.async copies into the
-//     same swizzled layout. 3 stages of 128 tokens either way. Stages are large
+//   - loaders fill a ring of stages through the page table (sparse gather,
+//     dense compute: overview ⑥, walkthrough §IV.2 and §V.4). Pages of 8 or
+//     more tokens: warp 4 (K) and warp 5 (V) issue one TMA tensor copy per page
+//     box (up to 64 rows of one kv head, 128-byte swizzle), page ids read 32
+//     boxes at a time one batch ahead. Smaller pages: 16-byte cp.async copies
+//     into the same swizzled layout by warps 4-7 (K: 4 and 5, V: 6 and 7, each
+//     one half of a stage's tokens: two warps per operand keep twice the copies
+//     in flight, 102 -> 89 us on the page-size-1 decode). 3 stages of 128
+//     tokens either way. Stages are large
 //     because each carries a fixed handshake cost. mbarriers carry the
 //     handshake (full: the stage's bytes / every lane's copies landed; empty:
 //     the compute warps are done with it); the ring runs across the CTA's work
@@ -61,7 +64,7 @@ constexpr int kDecThreads = 128;            // fp32 kernel
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMmaRows = 16;                 // fused heads per tile (M of the MMA)
 
-// bf16 kernel: warps 0..3 compute, warps 4 and 5 load K and V.
+// bf16 kernel: warps 0..3 compute, warps 4 and 5 (TMA) or 4..7 (cp.async) load K and V.
 constexpr int kConsumers = 4;
 constexpr int kTileK = 64;                   // unit of the stage sizes below; the largest page box (rows)
 constexpr int kStages = 5;
@@ -111,7 +114,8 @@ struct DecodeLayout {
     static constexpr int kCons = kFp8 ? 8 : 4;                               // compute warps
     static constexpr int kSubB = kTK / (16 * kCons);                         // 16-token sub-blocks per warp and stage
     static constexpr int kScrRows = kFp8 ? 8 * kNH : kMmaRows;               // scratch rows per warp
-    static constexpr int kThreads = 32 * (kCons + 2);
+    static constexpr int kLoad = kTma ? 2 : 4;                               // loader warps
+    static constexpr int kThreads = 32 * (kCons + kLoad);
     static constexpr int kElem = kFp8 ? 1 : 2;               // bytes per K/V element in the ring
     // Both gathers fill the same layout: [D * elem / 128 slabs][kTK rows][128 B],
     // 16-byte chunks XOR-swizzled by row (TMA's 128-byte swizzle; the cp.async
@@ -260,7 +264,7 @@ __global__ void wait_probe_kernel(long long limit_cycles, int *status) {
 
 // kNH (e4m3 only): 8-head tiles per kv head, ceil(g / 8)
 template <int D, bool kTma, bool kFp8 = false, int kNH = 1>
-__global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
+__global__ void __launch_bounds__(DecodeLayout<D, kTma, kFp8, kNH>::kThreads, 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const DecodeParams p) {
     static_assert(!kFp8 || (kTma && D == 128), "e4m3 pools: TMA gather, head_dim 128");
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
     sm100::fence_proxy_async_smem();
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            sm100::mbar_init(full0 + 8 * s, kTma ? 2 : 64);  // TMA: one per producer warp; else per lane
+            sm100::mbar_init(full0 + 8 * s, kTma ? 2 : 32 * LY::kLoad);  // TMA: one per producer warp; else per lane
             sm100::mbar_init(empty0 + 8 * s, kConsumers);
         }
         sm100::mbar_init(merge_in, kConsumers);
@@ -362,13 +366,16 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
         return;
     }
     if (!kTma && warp >= kConsumers) {
-        // ---------------- producers: warp 4 copies K rows, warp 5 V rows ----
-        // Each lane first turns the page ids of tokens `lane` and `lane + 32` of
-        // the stage into byte offsets of their rows (one division each), then
-        // every warp instruction copies T = 32 / C whole rows, C = D / 8 chunks
-        // of 16 bytes per row, taking the row offsets by shuffle.
+        // ---------------- producers: warps 4, 5 copy K rows, warps 6, 7 V rows ----
+        // Warp 4 (6) takes the first half of each stage's tokens, warp 5 (7) the
+        // second. Each lane first turns the page ids of its tokens `lane` and
+        // `lane + 32` of the half into byte offsets of their rows (one division
+        // each), then every warp instruction copies T = 32 / C whole rows, C =
+        // D / 8 chunks of 16 bytes per row, taking the row offsets by shuffle.
         constexpr int C = D / 8, T = 32 / C;
-        const bool is_v = warp == kConsumers + 1;
+        constexpr int kHalfTK = kTK / 2;  // tokens of a stage per loader warp
+        const bool is_v = warp >= kConsumers + 2;
+        const int tok_base = ((warp - kConsumers) & 1) * kHalfTK;
         const char *src = static_cast<const char *>(is_v ? p.v : p.k);
         const uint32_t part = is_v ? LY::kTileBytes : 0;
         const int my_chunk = lane % C, my_sub = lane / C;
@@ -377,14 +384,14 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
             const int nt = (len + kTK - 1) / kTK;
-            constexpr int kJ = kTK / 32;  // tokens per lane and stage
+            constexpr int kJ = kHalfTK / 32;  // tokens per lane and stage
             int pg[kJ];
 #pragma unroll
             for (int jj = 0; jj < kJ; ++jj) pg[jj] = 0;
             auto fetch = [&](int t, int (&dst)[kJ]) {
 #pragma unroll
                 for (int jj = 0; jj < kJ; ++jj) {
-                    const int j = lane + 32 * jj;
+                    const int j = tok_base + lane + 32 * jj;
                     const int tok = w.kv_start + t * kTK + j;
                     if (t * kTK + j < len) dst[jj] = __ldg(p.kv_indices + w.page_base + tok / p.page_size);
                 }
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 uint64_t off[kJ];
 #pragma unroll
                 for (int jj = 0; jj < kJ; ++jj) {
-                    const int tok = w.kv_start + t * kTK + lane + 32 * jj;
+                    const int tok = w.kv_start + t * kTK + tok_base + lane + 32 * jj;
                     off[jj] = (((uint64_t)pg[jj] * p.page_size + tok % p.page_size) * p.H_kv + w.kv_head) * (D * 2);
                 }
                 if (t + 1 < nt) fetch(t + 1, pg);
@@ -406,10 +413,11 @@ __global__ void __launch_bounds__(32 * ((kFp8 ? 8 : kConsumers) + 2), 1)
                 const int n = min(kTK, len - t * kTK);
                 const uint32_t dst = sbase + s * LY::kStageBytes + part;
 #pragma unroll
-                for (int i = 0; i < kTK / T; ++i) {
-                    const int j = i * T + my_sub;                     // token within the stage
+                for (int i = 0; i < kHalfTK / T; ++i) {
+                    const int jl = i * T + my_sub;                    // token within this warp's half
+                    const int j = tok_base + jl;                      // token within the stage
                     const int half = (i * T) >> 5;                    // same for the whole warp: T divides 32
-                    const uint64_t o = __shfl_sync(0xffffffffu, off[half], j & 31);
+                    const uint64_t o = __shfl_sync(0xffffffffu, off[half], jl & 31);
                     if (j < n) cp_async_16(dst + LY::chunk(j, my_chunk), src + o + my_chunk * 16, 16);
                 }
                 // arrive on full[s] once this lane's copies have landed
