@@ -32,6 +32,8 @@ CASES = [
     (10, [96, 250], [96, 700], 32, 8, 32, False, 5),                     # page 32 (two pages per box row set)
     (13, [150, 300], [400, 300], 32, 8, 64, True, 9),                    # 64-token pages
     (14, [77, 260], [1000, 260], 16, 4, 256, True, 11),                  # 256-token pages: a page spans two KV tiles
+    (15, [100, 0, 77], [300, 50, 77], 32, 2, 16, True, 9),              # g = 16 (16 positions per tile); a request without queries
+    (16, [0, 40, 0], [10, 200, 0], 16, 4, 16, False, 4),                 # non-causal; requests without queries or keys
 ]
 
 
