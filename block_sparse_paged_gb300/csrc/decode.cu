@@ -15,11 +15,11 @@
 //     into the same swizzled layout by warps 4-7 (K: 4 and 5, V: 6 and 7, each
 //     one half of a stage's tokens: two warps per operand keep twice the copies
 //     in flight, 102 -> 89 us on the page-size-1 decode). 3 stages of 128
-//     tokens either way. Stages are large
-//     because each carries a fixed handshake cost. mbarriers carry the
-//     handshake (full: the stage's bytes / every lane's copies landed; empty:
-//     the compute warps are done with it); the ring runs across the CTA's work
-//     items, so the next item's first stages load while the current one ends.
+//     tokens either way. Stages are large because each carries a fixed
+//     handshake cost. mbarriers carry the handshake (full: the stage's bytes /
+//     every lane's copies landed; empty: the compute warps are done with it);
+//     the ring runs across the CTA's work items, so the next item's first
+//     stages load while the current one ends.
 //   - compute (warps 0..3): each warp takes two 16-token sub-blocks per stage;
 //     S = Q K^T and O += P V on the warp-level tensor-core MMA (m16n8k16, rows
 //     = the g fused heads), fp32 online softmax in base 2 with the scale folded
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, kTma, kFp8, kNH>::kThreads, 1)
             const bsp_work_item w = items[it];
             const int len = w.kv_end - w.kv_start;
             const int nt = (len + kTK - 1) / kTK;
-            constexpr int kJ = kHalfTK / 32;  // tokens per lane and stage
+            constexpr int kJ = kHalfTK / 32;  // tokens per lane in this warp's half of a stage
             int pg[kJ];
 #pragma unroll
             for (int jj = 0; jj < kJ; ++jj) pg[jj] = 0;
